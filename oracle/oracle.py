@@ -1,0 +1,169 @@
+"""fp64 CPU oracle for the TwoTower denoiser step -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this module.  It wraps ``oracle.c`` (plain C, fp64,
+compiled with gcc) through ctypes and adds the block loop, which is plain
+Python around the per-step unmask.  It shares nothing with the CUDA library.
+
+Parity status of every function here is pinned by ``tests/test_oracle_pins.py``
+(closed forms, invariants, library special cases, brute force, planted mistakes).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Callable, Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+_p = ctypes.c_void_p
+_i = ctypes.c_int
+
+
+def build(out_path: str = _LIB_PATH, defines: tuple = ()) -> str:
+    """Compile oracle.c with gcc into a shared library; returns its path."""
+    cmd = ["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-pthread", "-Wall", "-Werror"]
+    cmd += [f"-D{d}" for d in defines]
+    cmd += [_SRC, "-o", out_path, "-lm"]
+    subprocess.run(cmd, check=True)
+    return out_path
+
+
+def _needs_build(path: str) -> bool:
+    return not os.path.exists(path) or os.path.getmtime(path) < os.path.getmtime(_SRC)
+
+
+def load(path: Optional[str] = None):
+    """Load (building when stale) the oracle library; returns the ctypes handle."""
+    global _lib
+    if path is None:
+        if _lib is not None:
+            return _lib
+        if _needs_build(_LIB_PATH):
+            build()
+        path = _LIB_PATH
+    lib = ctypes.CDLL(path)
+    lib.oracle_hw_threads.restype = _i
+    lib.oracle_block_attn.restype = _i
+    lib.oracle_block_attn.argtypes = [_i, _i, _i, _i, _i, _i, ctypes.c_double,
+                                      _p, _p, _p, _p, _p, _p, _p, _p, _i]
+    lib.oracle_confidence_unmask.restype = _i
+    lib.oracle_confidence_unmask.argtypes = [_i, _i, _i, _i, _p, ctypes.c_double, ctypes.c_float,
+                                             ctypes.c_int32, _i, _p, _p, _p, _p, _p, _p, _i]
+    if path == _LIB_PATH:
+        _lib = lib
+    return lib
+
+
+def hw_threads() -> int:
+    return load().oracle_hw_threads()
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def block_attn(q, k_ctx, v_ctx, ctx_lens, k_blk, v_blk, scale: float = 0.0,
+               nthreads: int = 0, lib=None, return_threads: bool = False):
+    """Exact block-query attention in fp64.
+
+    q [B,S,Hq,d], k_ctx/v_ctx [B,Hkv,Lmax,d], k_blk/v_blk [B,S,Hkv,d]: bf16 bit
+    patterns (uint16).  ctx_lens int32[B].  scale <= 0 means 1/sqrt(d).
+    Returns (out float64 [B,S,Hq,d], lse float64 [B,Hq,S]).
+    """
+    lib = lib or load()
+    q, k_blk, v_blk = _c(q, np.uint16), _c(k_blk, np.uint16), _c(v_blk, np.uint16)
+    k_ctx, v_ctx = _c(k_ctx, np.uint16), _c(v_ctx, np.uint16)
+    lens = _c(ctx_lens, np.int32)
+    B, S, Hq, d = q.shape
+    Hkv, Lmax = k_ctx.shape[1], k_ctx.shape[2]
+    out = np.empty((B, S, Hq, d), dtype=np.float64)
+    lse = np.empty((B, Hq, S), dtype=np.float64)
+    used = lib.oracle_block_attn(B, S, Hq, Hkv, d, Lmax, float(scale), _ptr(q), _ptr(k_ctx),
+                                 _ptr(v_ctx), _ptr(lens), _ptr(k_blk), _ptr(v_blk), _ptr(out),
+                                 _ptr(lse), int(nthreads))
+    if used < 0:
+        raise ValueError("oracle_block_attn: invalid arguments")
+    return (out, lse, used) if return_threads else (out, lse)
+
+
+def confidence_unmask(logits, dtype: str, temperature: float, threshold: float,
+                      mask_token_id: int, tokens, is_masked, force_commit_all: bool = False,
+                      nthreads: int = 0, lib=None) -> dict:
+    """One confidence-unmasking step (see oracle.c).  tokens/is_masked are copied.
+
+    Returns dict(tokens, is_masked, conf, committed_now, remaining, ambiguous, threads).
+    """
+    lib = lib or load()
+    if dtype not in ("f32", "bf16"):
+        raise ValueError(dtype)
+    lg = _c(logits, np.float32 if dtype == "f32" else np.uint16)
+    B, S, V = lg.shape
+    tok = np.array(tokens, dtype=np.int32, copy=True).reshape(B, S)
+    msk = np.array(is_masked, dtype=np.uint8, copy=True).reshape(B, S)
+    conf = np.empty((B, S), dtype=np.float64)
+    now = np.empty((B, S), dtype=np.uint8)
+    rem = np.empty((B,), dtype=np.int32)
+    amb = np.empty((B, S), dtype=np.uint8)
+    used = lib.oracle_confidence_unmask(B, S, V, 0 if dtype == "f32" else 1, _ptr(lg),
+                                        float(temperature), float(threshold), int(mask_token_id),
+                                        int(bool(force_commit_all)), _ptr(tok), _ptr(msk),
+                                        _ptr(conf), _ptr(now), _ptr(rem), _ptr(amb), int(nthreads))
+    if used < 0:
+        raise ValueError("oracle_confidence_unmask: invalid arguments")
+    return dict(tokens=tok, is_masked=msk, conf=conf, committed_now=now, remaining=rem,
+                ambiguous=amb, threads=used)
+
+
+def block_loop(B: int, S: int, logits_fn: Callable[[int], np.ndarray], dtype: str,
+               temperature: float, threshold: float, mask_token_id: int, steps_per_block: int,
+               start_step: int = 0, state: Optional[dict] = None,
+               stop_step: Optional[int] = None, nthreads: int = 0, lib=None) -> dict:
+    """In-block iteration of the denoiser step.
+
+    A block starts as S copies of mask_token_id, all masked.  For step k in
+    [start_step, stop_step) (stop_step defaults to steps_per_block): stop early
+    once nothing is masked; otherwise
+    take the step's logits from logits_fn(k) (the stand-in for the denoiser
+    forward), run one unmask step -- forcing every remaining position to commit
+    at the last step -- and count the step for each sequence that still had a
+    masked position.  ``state`` (tokens, is_masked, steps_used, committed_step)
+    resumes an interrupted loop.  Follows the block-by-block mechanism of the
+    dothoosh.com article (section "two-tower mechanism") and the generate
+    arguments of the 889990.xyz code example.
+    """
+    if state is None or start_step == 0:
+        tokens = np.full((B, S), mask_token_id, dtype=np.int32)
+        masked = np.ones((B, S), dtype=np.uint8)
+        steps_used = np.zeros((B,), dtype=np.int32)
+        committed_step = np.full((B, S), -1, dtype=np.int32)
+    else:
+        tokens = np.array(state["tokens"], dtype=np.int32, copy=True)
+        masked = np.array(state["is_masked"], dtype=np.uint8, copy=True)
+        steps_used = np.array(state["steps_used"], dtype=np.int32, copy=True)
+        committed_step = np.array(state["committed_step"], dtype=np.int32, copy=True)
+    ambiguous = 0
+    stop = steps_per_block if stop_step is None else min(stop_step, steps_per_block)
+    for k in range(start_step, stop):
+        active = masked.reshape(B, S).any(axis=1)
+        if not active.any():
+            break
+        r = confidence_unmask(logits_fn(k), dtype, temperature, threshold, mask_token_id,
+                              tokens, masked, force_commit_all=(k == steps_per_block - 1),
+                              nthreads=nthreads, lib=lib)
+        steps_used += active.astype(np.int32)
+        committed_step[r["committed_now"] == 1] = k
+        tokens, masked = r["tokens"], r["is_masked"]
+        ambiguous += int(r["ambiguous"].sum())
+    return dict(tokens=tokens, is_masked=masked, steps_used=steps_used,
+                committed_step=committed_step, ambiguous=ambiguous)
