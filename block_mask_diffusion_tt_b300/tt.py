@@ -1,0 +1,320 @@
+"""Thin ctypes binding of libtt (include/tt.h) taking torch CUDA tensors.
+
+Argument marshalling only: shapes and strides are read from the tensors, the
+raw device pointers and the current CUDA stream are passed to the C ABI, and a
+non-OK status raises ``TTError``.  Every step of the computation runs in the
+library's CUDA kernels; there is no fallback path, and loading fails loudly if
+libtt.so has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Callable, Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtt.so")
+
+TT_OK, TT_ERR_INVALID_ARG, TT_ERR_UNSUPPORTED, TT_ERR_WORKSPACE = 0, 1, 2, 3
+TT_ERR_CUDA, TT_ERR_TIMEOUT, TT_ERR_CALLBACK, TT_ERR_INTERNAL = 4, 5, 6, 7
+TT_F32, TT_BF16 = 0, 1
+SYNTH_MAX_STEPS = 256
+
+_i32 = ctypes.c_int32
+_p = ctypes.c_void_p
+_sz = ctypes.c_size_t
+_i64x4 = ctypes.c_int64 * 4
+
+
+class TTError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{status_string(status)}: {message}")
+        self.status = status
+
+
+class AttnDesc(ctypes.Structure):
+    _fields_ = [("B", _i32), ("S", _i32), ("Hq", _i32), ("Hkv", _i32), ("d", _i32),
+                ("Lmax", _i32), ("scale", ctypes.c_float), ("q_strides", _i64x4),
+                ("kctx_strides", _i64x4), ("vctx_strides", _i64x4), ("kblk_strides", _i64x4),
+                ("vblk_strides", _i64x4), ("o_strides", _i64x4)]
+
+
+class UnmaskDesc(ctypes.Structure):
+    _fields_ = [("B", _i32), ("S", _i32), ("V", _i32), ("logits_dtype", ctypes.c_int),
+                ("logits_row_stride", ctypes.c_int64), ("temperature", ctypes.c_float),
+                ("threshold", ctypes.c_float), ("mask_token_id", _i32)]
+
+
+class SynthParams(ctypes.Structure):
+    _fields_ = [("seed", ctypes.c_uint64), ("B", _i32), ("S", _i32), ("V", _i32),
+                ("dtype", ctypes.c_int), ("sigma", ctypes.c_float),
+                ("spike_threshold", ctypes.c_uint64 * SYNTH_MAX_STEPS)]
+
+
+LOGITS_FN = ctypes.CFUNCTYPE(ctypes.c_int, _p, _i32, _p, _p, _p, _p)
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Loads libtt.so (raises if it is missing: build it with build.py)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is not built; run `python -m block_mask_diffusion_tt_b300.build`")
+    lib = ctypes.CDLL(path)
+    sig = {
+        "tt_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "tt_last_error": (ctypes.c_char_p, []),
+        "tt_abi_version": (_i32, []),
+        "tt_workspace_zero": (ctypes.c_int, [_p, _sz, _p]),
+        "tt_block_attn_workspace_size": (_sz, [ctypes.POINTER(AttnDesc)]),
+        "tt_block_attn": (ctypes.c_int, [ctypes.POINTER(AttnDesc), _p, _p, _p, _p, _p, _p, _p, _p,
+                                         _p, _sz, _p]),
+        "tt_confidence_unmask_workspace_size": (_sz, [ctypes.POINTER(UnmaskDesc)]),
+        "tt_confidence_unmask": (ctypes.c_int, [ctypes.POINTER(UnmaskDesc), _p, _p, _p, _p, _p, _p,
+                                                _i32, _p, _sz, _p]),
+        "tt_denoise_block_loop_workspace_size": (_sz, [ctypes.POINTER(UnmaskDesc)]),
+        "tt_denoise_block_loop": (ctypes.c_int, [ctypes.POINTER(UnmaskDesc), _i32, _i32, _i32, _p,
+                                                 _p, _p, _p, _p, _p, _p, _p, _sz, _p, _i32,
+                                                 ctypes.POINTER(_i32)]),
+        "tt_synth_logits": (ctypes.c_int, [ctypes.c_uint64, _i32, _i32, _i32, _i32, ctypes.c_int,
+                                           ctypes.c_float, ctypes.c_uint64, _p, _p]),
+        "tt_synth_logits_producer": (ctypes.c_int, [_p, _i32, _p, _p, _p, _p]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(s: int) -> str:
+    try:
+        return load().tt_status_string(int(s)).decode()
+    except Exception:  # library unavailable while formatting an error
+        return f"status {s}"
+
+
+def last_error() -> str:
+    return load().tt_last_error().decode()
+
+
+def check(status: int):
+    if status != TT_OK:
+        raise TTError(status, last_error())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, ndim: Optional[int] = None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+
+
+class Workspace:
+    """A zeroed device workspace (uint8 tensor) sized by a *_workspace_size query."""
+
+    def __init__(self, nbytes: int, device=None):
+        if nbytes == 0:
+            raise TTError(TT_ERR_INVALID_ARG, last_error() or "workspace size query failed")
+        self.tensor = torch.zeros(int(nbytes) + 256, dtype=torch.uint8, device=device or "cuda")
+        off = (-self.tensor.data_ptr()) % 256
+        self.view = self.tensor[off:off + int(nbytes)]
+        self.nbytes = int(nbytes)
+
+    @property
+    def ptr(self):
+        return ctypes.c_void_p(self.view.data_ptr())
+
+
+# ------------------------------------------------------------------ attention
+def attn_desc(q, k_ctx, v_ctx, k_blk, v_blk, out, scale: float = 0.0) -> AttnDesc:
+    B, S, Hq, d = q.shape
+    Hkv, Lmax = k_ctx.shape[1], k_ctx.shape[2]
+    desc = AttnDesc(B=B, S=S, Hq=Hq, Hkv=Hkv, d=d, Lmax=Lmax, scale=float(scale))
+    desc.q_strides = _i64x4(*q.stride())
+    desc.kctx_strides = _i64x4(*k_ctx.stride())
+    desc.vctx_strides = _i64x4(*v_ctx.stride())
+    desc.kblk_strides = _i64x4(*k_blk.stride())
+    desc.vblk_strides = _i64x4(*v_blk.stride())
+    desc.o_strides = _i64x4(*out.stride())
+    return desc
+
+
+def block_attn_workspace_size(desc: AttnDesc) -> int:
+    return int(load().tt_block_attn_workspace_size(ctypes.byref(desc)))
+
+
+def block_attn(q, k_ctx, v_ctx, ctx_lens, k_blk, v_blk, out=None, lse=None, scale: float = 0.0,
+               workspace: Optional[Workspace] = None, stream=None):
+    """Block-query attention (tt_block_attn).  bf16 tensors, ctx_lens int32[B].
+
+    Returns out [B,S,Hq,d] bf16 (and writes lse [B,Hq,S] fp32 when given).
+    """
+    for t, n, nd in ((q, "q", 4), (k_ctx, "k_ctx", 4), (v_ctx, "v_ctx", 4), (k_blk, "k_blk", 4),
+                     (v_blk, "v_blk", 4)):
+        _need(t, n, torch.bfloat16, nd)
+    _need(ctx_lens, "ctx_lens", torch.int32, 1)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    _need(out, "out", torch.bfloat16, 4)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 3)
+    desc = attn_desc(q, k_ctx, v_ctx, k_blk, v_blk, out, scale)
+    if workspace is None:
+        workspace = Workspace(block_attn_workspace_size(desc), q.device)
+    check(load().tt_block_attn(ctypes.byref(desc), _ptr(q), _ptr(k_ctx), _ptr(v_ctx),
+                               _ptr(ctx_lens), _ptr(k_blk), _ptr(v_blk), _ptr(out), _ptr(lse),
+                               workspace.ptr, workspace.nbytes, _stream(stream)))
+    return out
+
+
+# ------------------------------------------------------------------ unmasking
+def unmask_desc(B, S, V, dtype, temperature, threshold, mask_token_id, row_stride=0) -> UnmaskDesc:
+    return UnmaskDesc(B=B, S=S, V=V, logits_dtype=dtype, logits_row_stride=row_stride,
+                      temperature=float(temperature), threshold=float(threshold),
+                      mask_token_id=int(mask_token_id))
+
+
+def _logits_dtype(logits: torch.Tensor) -> int:
+    if logits.dtype == torch.float32:
+        return TT_F32
+    if logits.dtype == torch.bfloat16:
+        return TT_BF16
+    raise TypeError("logits must be float32 or bfloat16")
+
+
+def _row_stride(logits: torch.Tensor) -> int:
+    B, S, V = logits.shape
+    rs = logits.stride(1) if S > 1 else logits.stride(0)
+    if logits.stride(2) != 1 or (B > 1 and S > 1 and logits.stride(0) != S * rs):
+        raise ValueError("logits must be [B,S,V] with a uniform row stride and contiguous V")
+    return rs
+
+
+def confidence_unmask_workspace_size(desc: UnmaskDesc) -> int:
+    return int(load().tt_confidence_unmask_workspace_size(ctypes.byref(desc)))
+
+
+def confidence_unmask(logits, tokens, is_masked, temperature: float, threshold: float,
+                      mask_token_id: int, force_commit_all: bool = False, conf=None,
+                      committed_now=None, remaining=None, workspace: Optional[Workspace] = None,
+                      stream=None) -> dict:
+    """One confidence-unmasking step (tt_confidence_unmask); tokens/is_masked updated in place."""
+    if logits.dim() != 3:
+        raise ValueError("logits must be [B,S,V]")
+    B, S, V = logits.shape
+    _need(tokens, "tokens", torch.int32, 2)
+    _need(is_masked, "is_masked", torch.uint8, 2)
+    dev = logits.device
+    conf = torch.empty((B, S), dtype=torch.float32, device=dev) if conf is None else conf
+    committed_now = (torch.empty((B, S), dtype=torch.uint8, device=dev)
+                     if committed_now is None else committed_now)
+    remaining = torch.empty((B,), dtype=torch.int32, device=dev) if remaining is None else remaining
+    desc = unmask_desc(B, S, V, _logits_dtype(logits), temperature, threshold, mask_token_id,
+                       _row_stride(logits))
+    if workspace is None:
+        workspace = Workspace(confidence_unmask_workspace_size(desc), dev)
+    check(load().tt_confidence_unmask(ctypes.byref(desc), _ptr(logits), _ptr(tokens),
+                                      _ptr(is_masked), _ptr(conf), _ptr(committed_now),
+                                      _ptr(remaining), int(bool(force_commit_all)), workspace.ptr,
+                                      workspace.nbytes, _stream(stream)))
+    return dict(tokens=tokens, is_masked=is_masked, conf=conf, committed_now=committed_now,
+                remaining=remaining)
+
+
+# ------------------------------------------------------------------ loop and synthetic logits
+def synth_logits(seed: int, step: int, B: int, S: int, V: int, sigma: float, spike_threshold: int,
+                 dtype: int = TT_BF16, out=None, stream=None):
+    """Counter-based synthetic logits on the device (tt_synth_logits)."""
+    if out is None:
+        out = torch.empty((B, S, V), dtype=torch.bfloat16 if dtype == TT_BF16 else torch.float32,
+                          device="cuda")
+    check(load().tt_synth_logits(int(seed), int(step), B, S, V, int(dtype), float(sigma),
+                                 int(spike_threshold), _ptr(out), _stream(stream)))
+    return out
+
+
+def synth_params(seed: int, B: int, S: int, V: int, dtype: int, sigma: float,
+                 thresholds) -> SynthParams:
+    p = SynthParams(seed=int(seed), B=B, S=S, V=V, dtype=int(dtype), sigma=float(sigma))
+    thr = list(thresholds)
+    for i in range(SYNTH_MAX_STEPS):
+        p.spike_threshold[i] = int(thr[min(i, len(thr) - 1)]) if thr else 0
+    return p
+
+
+def denoise_block_loop_workspace_size(desc: UnmaskDesc) -> int:
+    return int(load().tt_denoise_block_loop_workspace_size(ctypes.byref(desc)))
+
+
+def denoise_block_loop(B: int, S: int, V: int, logits_dtype: int, temperature: float,
+                       threshold: float, mask_token_id: int, steps_per_block: int,
+                       tokens, is_masked, steps_used, committed_step=None, logits_buf=None,
+                       producer: Optional[Callable] = None, synth: Optional[SynthParams] = None,
+                       start_step: int = 0, stop_step: int = 0, timeout_ms: int = 60000,
+                       workspace: Optional[Workspace] = None, stream=None) -> int:
+    """In-block loop (tt_denoise_block_loop); returns the number of steps run.
+
+    Exactly one of ``producer`` (a Python callable ``f(step, logits_buf)`` that
+    fills the logits tensor on the current stream) or ``synth`` (parameters of
+    the library's own synthetic producer) gives each step's logits.
+    """
+    lib = load()
+    dt = torch.bfloat16 if logits_dtype == TT_BF16 else torch.float32
+    if logits_buf is None:
+        logits_buf = torch.empty((B, S, V), dtype=dt, device="cuda")
+    desc = unmask_desc(B, S, V, logits_dtype, temperature, threshold, mask_token_id)
+    if workspace is None:
+        workspace = Workspace(denoise_block_loop_workspace_size(desc))
+    keep = []
+    if synth is not None:
+        fn_ptr = ctypes.cast(lib.tt_synth_logits_producer, _p)
+        user = ctypes.cast(ctypes.pointer(synth), _p)
+    elif producer is not None:
+        def _cb(_user, step, _tok, _msk, _out, _stream_handle):
+            try:
+                producer(int(step), logits_buf)
+                return TT_OK
+            except Exception:  # reported as TT_ERR_CALLBACK by the loop
+                return TT_ERR_INTERNAL
+        cb = LOGITS_FN(_cb)
+        keep.append(cb)
+        fn_ptr = ctypes.cast(cb, _p)
+        user = None
+    else:
+        raise ValueError("need producer or synth")
+    steps_run = _i32(0)
+    status = lib.tt_denoise_block_loop(ctypes.byref(desc), steps_per_block, start_step, stop_step,
+                                       fn_ptr, user, _ptr(logits_buf), _ptr(tokens),
+                                       _ptr(is_masked), _ptr(steps_used), _ptr(committed_step),
+                                       workspace.ptr, workspace.nbytes, _stream(stream),
+                                       int(timeout_ms), ctypes.byref(steps_run))
+    del keep
+    check(status)
+    return int(steps_run.value)
+
+
+def exported_symbols() -> list:
+    """Names of the entry points this binding expects libtt.so to export."""
+    return ["tt_status_string", "tt_last_error", "tt_abi_version", "tt_workspace_zero",
+            "tt_block_attn_workspace_size", "tt_block_attn", "tt_confidence_unmask_workspace_size",
+            "tt_confidence_unmask", "tt_denoise_block_loop_workspace_size", "tt_denoise_block_loop",
+            "tt_synth_logits", "tt_synth_logits_producer"]

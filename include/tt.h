@@ -1,0 +1,277 @@
+/*
+ * tt.h -- C ABI of libtt: the denoiser-step hot path of the TwoTower block
+ * mask-diffusion decoder on one NVIDIA B300 (sm_103a).
+ *
+ * Two operations, and the in-block loop that iterates the second:
+ *
+ *  tt_block_attn         block-query attention of one denoiser attention layer.
+ *                        The S block queries of layer i attend, through one
+ *                        softmax with grouped-query heads, to context-tower
+ *                        layer i's K/V for the committed prefix plus the block's
+ *                        own K/V, bidirectionally inside the block.
+ *                        Pages: dothoosh.com, "فرآیند انتشار در برابر رمزگشایی
+ *                        متوالی در مدل جدید انویدیا", section "two-tower mechanism"
+ *                        (bidirectional within the block, causal to earlier clean
+ *                        blocks, layer i coupled to layer i); aitrends.kr,
+ *                        "Nemotron-Labs-TwoTower-30B-A3B-Base-BF16", section
+ *                        "technical features" (layer-aligned attention to the
+ *                        context tower's KV); tgviewer.app, "NVIDIA, возможно,
+ *                        решила главный компромисс современных LLM" (layer-by-layer
+ *                        coupling of the towers).
+ *
+ *  tt_confidence_unmask  one confidence-unmasking step: per still-masked block
+ *                        position, the argmax token of the logits and the
+ *                        confidence max softmax(logits/T); commit every position
+ *                        with confidence >= gamma (at least the single most
+ *                        confident one) and re-mask the rest.
+ *                        Pages: keyframe.defihacklabs.io, "Diffusion Nemotron",
+ *                        key point 3; 889990.xyz, "NVIDIA发布Nemotron两塔模型",
+ *                        code example (temperature, confidence_threshold,
+ *                        mask_token_id, block_size, steps_per_block).
+ *
+ *  tt_denoise_block_loop the in-block iteration: a block starts as S mask tokens
+ *                        and is refined step by step until every position is
+ *                        committed (dothoosh.com article, "two-tower mechanism").
+ *
+ * Conventions for every entry point:
+ *  - All pointers named device are CUDA device pointers (global memory) that
+ *    the caller allocates, owns and keeps alive until the stream work ends.
+ *    Host pointers are named so.  The library allocates no device memory on any
+ *    call; scratch comes from the caller through the *_workspace_size queries.
+ *  - Work is enqueued asynchronously on `stream` (NULL = the legacy default
+ *    stream).  Only tt_denoise_block_loop waits on the host, once per step,
+ *    bounded by its timeout.
+ *  - Every call returns a tt_status and never aborts the process.  Arguments
+ *    are validated on the host before any launch; on TT_ERR_INVALID_ARG,
+ *    TT_ERR_UNSUPPORTED or TT_ERR_WORKSPACE nothing was enqueued.
+ *    tt_last_error() gives a message for the calling thread's last failure.
+ *  - Workspaces hold arrival counters that must be zero before a workspace's
+ *    first use: zero it once (tt_workspace_zero or any memset) after allocating
+ *    it.  Every successful call leaves the counters at zero again.  Calls that
+ *    share a workspace must be ordered on one stream.
+ *  - bf16 is IEEE bfloat16 bit patterns (uint16).  Strides are in elements.
+ */
+#ifndef TT_H_
+#define TT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (CUstream) handle; NULL selects the legacy default stream. */
+typedef struct CUstream_st *tt_stream_t;
+
+typedef enum {
+    TT_OK = 0,
+    TT_ERR_INVALID_ARG = 1,  /* bad shape, null pointer, negative size, T <= 0 ... */
+    TT_ERR_UNSUPPORTED = 2,  /* valid but outside what the kernels implement */
+    TT_ERR_WORKSPACE = 3,    /* workspace missing, too small or misaligned */
+    TT_ERR_CUDA = 4,         /* a CUDA runtime or launch error (message kept) */
+    TT_ERR_TIMEOUT = 5,      /* the loop's bounded wait on the device ran out */
+    TT_ERR_CALLBACK = 6,     /* the loop's logits producer returned non-OK */
+    TT_ERR_INTERNAL = 7
+} tt_status;
+
+typedef enum { TT_F32 = 0, TT_BF16 = 1 } tt_dtype;
+
+/* Static string naming a status. */
+const char *tt_status_string(tt_status s);
+/* Message of the calling thread's last non-OK status ("" if none).  Valid until
+ * the thread's next call into the library. */
+const char *tt_last_error(void);
+/* ABI version of this header (major*1000 + minor). */
+int32_t tt_abi_version(void);
+
+/* Enqueues a zero fill of `bytes` bytes of a device workspace.  Call once after
+ * allocating a workspace, before its first use. */
+tt_status tt_workspace_zero(void *workspace, size_t bytes, tt_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Block-query attention                                                     */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Shape and layout of one attention-layer call.
+ *   B     sequences;  S  block size (1..64);  Hq query heads;  Hkv KV heads
+ *         (Hq % Hkv == 0; query head h uses KV head h / (Hq/Hkv));
+ *   d     head dim, 64 or 128;  Lmax  allocated prefix rows of the context cache.
+ *   scale softmax scale; <= 0 selects 1/sqrt(d).
+ * Tensors (element strides, innermost dimension contiguous, i.e. stride 1;
+ * other strides positive multiples of 8 elements so rows start on 16 bytes):
+ *   q      [B, S, Hq, d]      bf16   block queries
+ *   k_ctx  [B, Hkv, Lmax, d]  bf16   context-tower layer-i keys (prefix rows
+ *   v_ctx  [B, Hkv, Lmax, d]  bf16   0..L_b-1 are read; rows >= L_b never are)
+ *   k_blk  [B, S, Hkv, d]     bf16   the block's own keys and values
+ *   v_blk  [B, S, Hkv, d]     bf16
+ *   out    [B, S, Hq, d]      bf16   written, round-to-nearest-even of fp32
+ */
+typedef struct {
+    int32_t B, S, Hq, Hkv, d, Lmax;
+    float scale;
+    int64_t q_strides[4];
+    int64_t kctx_strides[4];
+    int64_t vctx_strides[4];
+    int64_t kblk_strides[4];
+    int64_t vblk_strides[4];
+    int64_t o_strides[4];
+} tt_attn_desc;
+
+/* Bytes of device workspace tt_block_attn needs for `desc` on the current
+ * device (depends on B, Hkv, S*Hq/Hkv, d and the device's SM count; not on the
+ * context lengths).  0 on invalid desc. */
+size_t tt_block_attn_workspace_size(const tt_attn_desc *desc);
+
+/*
+ * out[b,s,h,:] = sum over keys j of softmax_j(scale * <q[b,s,h,:], key_j>) * value_j,
+ * where the keys of sequence b and KV head g = h/(Hq/Hkv) are the prefix rows
+ * k_ctx[b,g,0..L_b-1,:] followed by the block rows k_blk[b,0..S-1,g,:] (values
+ * alike).  Every block query sees the whole prefix and all S block keys.
+ *   ctx_lens  device int32[B], 0 <= L_b <= Lmax (not checked on the host; a
+ *             value outside that range is clamped into it by the kernel).
+ *   lse       device float[B, Hq, S] natural-log log-sum-exp of the scaled
+ *             scores, or NULL.
+ *   workspace device, >= tt_block_attn_workspace_size(desc) bytes, 256-byte
+ *             aligned, zeroed before first use (see conventions).
+ * The kernels split long prefixes across SMs and merge the partial softmax
+ * states with a log-sum-exp merge; the result does not depend on the split
+ * beyond fp32 rounding.
+ */
+tt_status tt_block_attn(const tt_attn_desc *desc, const void *q, const void *k_ctx,
+                        const void *v_ctx, const int32_t *ctx_lens, const void *k_blk,
+                        const void *v_blk, void *out, float *lse, void *workspace,
+                        size_t workspace_bytes, tt_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Confidence unmasking                                                      */
+/* ------------------------------------------------------------------------ */
+
+/*
+ *   B, S, V          sequences, block size (1..64), vocabulary size (>= 1)
+ *   logits_dtype     TT_F32 or TT_BF16
+ *   logits_row_stride elements between consecutive (b,s) rows; 0 means V
+ *   temperature      T > 0; confidence = max_v softmax(logits/T)_v
+ *   threshold        gamma: commit every masked position whose fp32
+ *                    confidence is >= gamma.  gamma = 0 commits all; gamma > 1
+ *                    commits exactly the single most confident one per step.
+ *   mask_token_id    token written into positions that stay masked
+ */
+typedef struct {
+    int32_t B, S, V;
+    tt_dtype logits_dtype;
+    int64_t logits_row_stride;
+    float temperature;
+    float threshold;
+    int32_t mask_token_id;
+} tt_unmask_desc;
+
+/* Bytes of device workspace tt_confidence_unmask needs (0 on invalid desc). */
+size_t tt_confidence_unmask_workspace_size(const tt_unmask_desc *desc);
+
+/*
+ * One unmasking step over device logits [B, S, V] (row stride as in desc; the
+ * base and each row must start on a 4-byte boundary).  For each sequence b:
+ *   for masked s: token = lowest index of the maximum raw logit;
+ *                 conf  = 1 / sum_v exp((l_v - max)/T)   (fp32);
+ *   commit C = { masked s : conf >= gamma }; if C is empty and a position is
+ *   masked, C = { the masked s of highest conf, lowest s on ties };
+ *   force_commit_all != 0 commits every masked position.
+ *   s in C:        tokens[b,s] = token, is_masked[b,s] = 0, committed_now = 1
+ *   masked, not C: tokens[b,s] = mask_token_id, committed_now = 0
+ *   not masked:    tokens unchanged, committed_now = 0, conf = NaN
+ * Device arrays:  tokens int32[B,S] and is_masked uint8[B,S] (in/out);
+ * conf float[B,S], committed_now uint8[B,S], remaining int32[B] (masked
+ * positions left) are written.  Only masked rows of logits are read.
+ * Rows must hold finite values or -inf with at least one finite value.
+ */
+tt_status tt_confidence_unmask(const tt_unmask_desc *desc, const void *logits, int32_t *tokens,
+                               uint8_t *is_masked, float *conf, uint8_t *committed_now,
+                               int32_t *remaining, int32_t force_commit_all, void *workspace,
+                               size_t workspace_bytes, tt_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* In-block loop                                                             */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Producer of one step's logits (the denoiser forward, or a stand-in).  It
+ * must enqueue on `stream` work that writes logits [B,S,V] (layout of the
+ * loop's desc) into logits_out, and may read tokens / is_masked (device).  A
+ * non-OK return stops the loop with TT_ERR_CALLBACK.
+ */
+typedef tt_status (*tt_logits_fn)(void *user, int32_t step, const int32_t *tokens,
+                                  const uint8_t *is_masked, void *logits_out,
+                                  tt_stream_t stream);
+
+/* Bytes of device workspace tt_denoise_block_loop needs (0 on invalid desc). */
+size_t tt_denoise_block_loop_workspace_size(const tt_unmask_desc *desc);
+
+/*
+ * Runs steps k = start_step .. min(stop_step, steps_per_block)-1 of the
+ * in-block iteration (stop_step <= 0 means steps_per_block):
+ *   if start_step == 0 the block is initialised first: tokens = mask_token_id,
+ *   is_masked = 1, steps_used = 0, committed_step = -1;
+ *   each step: if no position of any sequence is masked, stop; else
+ *   producer(user, k, ...) writes logits_buf, then one tt_confidence_unmask
+ *   step runs with force_commit_all at k == steps_per_block-1, steps_used[b]
+ *   grows by one for each b that had a masked position, and committed_step[b,s]
+ *   = k for positions committed at step k.
+ * A resumed call (start_step > 0) continues from the device state it is given,
+ * so running steps [0,a) then [a,n) equals running [0,n) bit for bit.
+ * Device arrays: tokens int32[B,S], is_masked uint8[B,S], steps_used int32[B],
+ * committed_step int32[B,S] (nullable) -- all in/out.  logits_buf is device
+ * memory for [B,S,V] logits.  After each step the host waits (polling, at most
+ * timeout_ms milliseconds, <= 0 = 60000) for the step's remaining counts;
+ * running out returns TT_ERR_TIMEOUT with the state of the last finished step.
+ * steps_run (host, nullable) receives the number of steps executed.
+ */
+tt_status tt_denoise_block_loop(const tt_unmask_desc *desc, int32_t steps_per_block,
+                                int32_t start_step, int32_t stop_step, tt_logits_fn producer,
+                                void *user, void *logits_buf, int32_t *tokens,
+                                uint8_t *is_masked, int32_t *steps_used, int32_t *committed_step,
+                                void *workspace, size_t workspace_bytes, tt_stream_t stream,
+                                int32_t timeout_ms, int32_t *steps_run);
+
+/* ------------------------------------------------------------------------ */
+/* Synthetic logits (a stand-in producer for benches and tests)              */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Counter-based synthetic logits, the same definition as the Python input
+ * generator: with SplitMix64's output function mix64 (Steele, Lea & Flood,
+ * OOPSLA 2014) and GAMMA = 0x9E3779B97F4A7C15,
+ *   key   = mix64(mix64(seed ^ 0x6C6F67697473) + (step+1)*GAMMA)
+ *   word  = mix64(key + (n+1)*GAMMA),  n = ((b*S+s)*V + v)*3 + j,  j = 0,1,2
+ *   z     = (sum of the twelve 16-bit fields of the three words - 393216)
+ *           * (sigma / 65536)     (fp32, exact)
+ *   spike: w = mix64(mix64(key ^ 0x7370696B65) + (b*S+s+1)*GAMMA); if
+ *          (w >> 32) < spike_threshold the row gets +8 at token (w & 0xFFFFFFFF) % V
+ *   bf16 output rounds the fp32 value to nearest-even.
+ * sigma/65536 must be exact in fp32.  out: device [B,S,V], row stride V.
+ */
+tt_status tt_synth_logits(uint64_t seed, int32_t step, int32_t B, int32_t S, int32_t V,
+                          tt_dtype dtype, float sigma, uint64_t spike_threshold, void *out,
+                          tt_stream_t stream);
+
+/* Parameters of tt_synth_logits_producer: the per-step spike threshold is
+ * spike_threshold[min(step, TT_SYNTH_MAX_STEPS-1)]. */
+#define TT_SYNTH_MAX_STEPS 256
+typedef struct {
+    uint64_t seed;
+    int32_t B, S, V;
+    tt_dtype dtype;
+    float sigma;
+    uint64_t spike_threshold[TT_SYNTH_MAX_STEPS];
+} tt_synth_params;
+
+/* A tt_logits_fn that calls tt_synth_logits with (tt_synth_params*)user. */
+tt_status tt_synth_logits_producer(void *user, int32_t step, const int32_t *tokens,
+                                   const uint8_t *is_masked, void *logits_out,
+                                   tt_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TT_H_ */

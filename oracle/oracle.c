@@ -184,6 +184,12 @@ int oracle_block_attn(int B, int S, int Hq, int Hkv, int d, int Lmax, double sca
 
 #define ORACLE_AMBIG_REL 1e-5
 
+/* A confidence within 2^-26 of 1 is exactly 1.0f in any fp32 evaluation whose
+ * relative error stays below 2^-25: the probability mass outside the top token
+ * is then under half an fp32 unit of the sum's leading 1.  Decisions between
+ * such confidences (exact fp32 ties, or a threshold of 1) are not ambiguous. */
+static int conf_is_one_in_f32(double c) { return c >= 1.0 - ldexp(1.0, -26); }
+
 struct unmask_ctx {
     int S, V, dtype;
     const void *logits;
@@ -234,7 +240,9 @@ static void unmask_row(void *p, long row)
  * remaining[b] = masked positions left.  ambiguous[b,s] (nullable) flags a
  * decision that a relative perturbation of 1e-5 in a confidence could flip:
  * |conf - threshold| <= 1e-5*threshold, or a fallback choice whose two best
- * confidences are within 1e-5 relative.  Returns threads used, -1 on bad args.
+ * confidences are within 1e-5 relative -- except between confidences that are
+ * 1.0f in any fp32 evaluation (conf_is_one_in_f32).  Returns threads used, -1
+ * on bad args.
  */
 int oracle_confidence_unmask(int B, int S, int V, int dtype, const void *logits,
                              double temperature, float threshold, int32_t mask_token_id,
@@ -262,7 +270,7 @@ int oracle_confidence_unmask(int B, int S, int V, int dtype, const void *logits,
                 committed_now[base + s] = 1;
                 ++n_pass;
             }
-            if (ambiguous && !force_commit_all &&
+            if (ambiguous && !force_commit_all && !conf_is_one_in_f32(conf[base + s]) &&
                 fabs(conf[base + s] - (double)threshold) <= ORACLE_AMBIG_REL * fabs((double)threshold))
                 ambiguous[base + s] = 1;
         }
@@ -276,6 +284,7 @@ int oracle_confidence_unmask(int B, int S, int V, int dtype, const void *logits,
             }
             committed_now[base + best] = 1;
             if (ambiguous && second >= 0 &&
+                !(conf_is_one_in_f32(conf[base + best]) && conf_is_one_in_f32(conf[base + second])) &&
                 fabs(conf[base + best] - conf[base + second]) <= ORACLE_AMBIG_REL * conf[base + best]) {
                 ambiguous[base + best] = 1;
                 ambiguous[base + second] = 1;

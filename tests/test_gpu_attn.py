@@ -1,0 +1,128 @@
+"""GPU parity of tt_block_attn against the fp64 oracle.
+
+Tolerances: max-abs 1.5e-2 and mean-abs 2e-3 on the bf16 output, 1e-4 absolute on
+the log-sum-exp.  Small cases are compared element by element over every output;
+the full-size workloads run in the launch configuration the bench times and are
+compared on sampled sequences (all heads and block rows of each).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_mask_diffusion_tt_b300 import synth, tt
+import _gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def test_tiny_config():
+    w = synth.workloads()["tiny"]
+    _gpu.check_attn(synth.attn_inputs(w.attn, seed=w.seed), what="tiny")
+
+
+@pytest.mark.parametrize("lens", [[0], [1], [63], [64], [65], [200, 7, 0, 129], [1000, 1, 64]])
+@pytest.mark.parametrize("d", [64, 128])
+def test_ragged_prefix_lengths(lens, d):
+    shape = synth.AttnShape(len(lens), 16, 8, 2, d, max(max(lens), 1), lens=lens)
+    _gpu.check_attn(synth.attn_inputs(shape, seed=sum(lens) + d), what=f"lens={lens} d={d}")
+
+
+@pytest.mark.parametrize("S,Hq,Hkv", [(1, 4, 4), (4, 32, 2), (16, 32, 2), (16, 32, 1), (32, 32, 2),
+                                      (64, 32, 2), (7, 12, 3), (16, 16, 16)])
+def test_block_sizes_and_head_groups(S, Hq, Hkv):
+    # S*Hq/Hkv above 256 spans several row groups
+    shape = synth.AttnShape(2, S, Hq, Hkv, 128, 300, lens=[300, 77])
+    _gpu.check_attn(synth.attn_inputs(shape, seed=S * 100 + Hq), what=f"S={S} Hq={Hq} Hkv={Hkv}")
+
+
+def test_nan_padding_is_never_read():
+    shape = synth.AttnShape(3, 16, 8, 2, 128, 512, lens=[512, 100, 0])
+    inp = synth.attn_inputs(shape, seed=3, nan_pad=True)
+    _gpu.check_attn(inp, what="nan padded")
+
+
+def test_explicit_scale():
+    shape = synth.AttnShape(2, 16, 8, 2, 64, 100, lens=[100, 50])
+    _gpu.check_attn(synth.attn_inputs(shape, seed=4), scale=0.05, what="scale")
+
+
+def test_many_splits_one_long_sequence():
+    # one pair spread over every SM: exercises the multi-part merge
+    shape = synth.AttnShape(1, 16, 16, 1, 128, 40000, lens=[40000])
+    _gpu.check_attn(synth.attn_inputs(shape, seed=5), what="long single")
+
+
+def test_strided_views():
+    """q taken from a fused [B,S,Hq+2Hkv,d] projection, caches inside larger buffers."""
+    B, S, Hq, Hkv, d, L = 2, 16, 8, 2, 128, 200
+    inp = synth.attn_inputs(synth.AttnShape(B, S, Hq, Hkv, d, L, lens=[200, 33]), seed=6)
+    ref, ref_lse = oracle.block_attn(inp["q"], inp["k_ctx"], inp["v_ctx"], inp["ctx_lens"],
+                                     inp["k_blk"], inp["v_blk"])
+    fused = torch.zeros((B, S, Hq + 2 * Hkv, d), dtype=torch.bfloat16, device=_gpu.DEV)
+    fused[:, :, :Hq] = _gpu.bf16_dev(inp["q"])
+    fused[:, :, Hq:Hq + Hkv] = _gpu.bf16_dev(inp["k_blk"])
+    fused[:, :, Hq + Hkv:] = _gpu.bf16_dev(inp["v_blk"])
+    big_k = torch.zeros((B, Hkv, L + 40, d), dtype=torch.bfloat16, device=_gpu.DEV)
+    big_v = torch.zeros((B, Hkv, L + 40, d), dtype=torch.bfloat16, device=_gpu.DEV)
+    big_k[:, :, :L] = _gpu.bf16_dev(inp["k_ctx"])
+    big_v[:, :, :L] = _gpu.bf16_dev(inp["v_ctx"])
+    out_big = torch.zeros((B, S, Hq + 4, d), dtype=torch.bfloat16, device=_gpu.DEV)
+    lens = torch.from_numpy(inp["ctx_lens"]).to(_gpu.DEV)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device=_gpu.DEV)
+    tt.block_attn(fused[:, :, :Hq], big_k, big_v, lens, fused[:, :, Hq:Hq + Hkv],
+                  fused[:, :, Hq + Hkv:], out=out_big[:, :, 2:2 + Hq], lse=lse)
+    torch.cuda.synchronize()
+    got = out_big[:, :, 2:2 + Hq].float().cpu().numpy().astype(np.float64)
+    _gpu.assert_attn_close(got, ref, lse.cpu().numpy(), ref_lse, "strided")
+    assert (out_big[:, :, :2] == 0).all() and (out_big[:, :, 2 + Hq:] == 0).all()
+
+
+def test_lse_optional_and_workspace_reuse():
+    shape = synth.AttnShape(4, 16, 32, 2, 128, 3000, lens=[3000, 1200, 64, 2999])
+    inp = synth.attn_inputs(shape, seed=7)
+    d = _gpu.attn_dev(inp)
+    desc = tt.attn_desc(d["q"], d["k_ctx"], d["v_ctx"], d["k_blk"], d["v_blk"], d["q"])
+    ws = tt.Workspace(tt.block_attn_workspace_size(desc))
+    ref, _ = oracle.block_attn(inp["q"], inp["k_ctx"], inp["v_ctx"], inp["ctx_lens"],
+                               inp["k_blk"], inp["v_blk"])
+    for _ in range(3):
+        out = tt.block_attn(d["q"], d["k_ctx"], d["v_ctx"], d["ctx_lens"], d["k_blk"], d["v_blk"],
+                            workspace=ws)
+        torch.cuda.synchronize()
+        _gpu.assert_attn_close(out.float().cpu().numpy().astype(np.float64), ref, what="reuse")
+
+
+def test_empty_batch():
+    z = torch.zeros((0, 16, 8, 128), dtype=torch.bfloat16, device=_gpu.DEV)
+    kv = torch.zeros((0, 2, 10, 128), dtype=torch.bfloat16, device=_gpu.DEV)
+    blk = torch.zeros((0, 16, 2, 128), dtype=torch.bfloat16, device=_gpu.DEV)
+    lens = torch.zeros((0,), dtype=torch.int32, device=_gpu.DEV)
+    tt.block_attn(z, kv, kv, lens, blk, blk, workspace=tt.Workspace(256))
+
+
+def _sampled_full_size(name, sample_b):
+    w = synth.workloads()[name]
+    inp = synth.attn_inputs(w.attn, seed=w.seed)
+    out, lse = _gpu.run_attn(inp)
+    for b in sample_b(inp["ctx_lens"]):
+        sub = {k: inp[k][b:b + 1] for k in ("q", "k_ctx", "v_ctx", "k_blk", "v_blk", "ctx_lens")}
+        L = int(sub["ctx_lens"][0])
+        sub["k_ctx"] = sub["k_ctx"][:, :, :max(L, 1)]
+        sub["v_ctx"] = sub["v_ctx"][:, :, :max(L, 1)]
+        ref, ref_lse = oracle.block_attn(**{k: sub[k] for k in ("q", "k_ctx", "v_ctx", "ctx_lens",
+                                                                "k_blk", "v_blk")})
+        _gpu.assert_attn_close(out[b:b + 1], ref, lse[b:b + 1], ref_lse, f"{name} b={b}")
+
+
+def test_full_size_default_sampled():
+    _sampled_full_size("default", lambda lens: [0, 5])
+
+
+def test_full_size_ragged16k_sampled():
+    _sampled_full_size("ragged16k", lambda lens: sorted({int(np.argmin(lens)), int(np.argmax(lens)),
+                                                         7}))
+
+
+def test_full_size_long_sampled():
+    _sampled_full_size("long", lambda lens: [2])
