@@ -1,4 +1,5 @@
 """The fp64 oracle against closed forms, invariants, library special cases and worked examples."""
+import numpy as np
 import pytest
 
 import oracle
