@@ -1,0 +1,452 @@
+#!/usr/bin/env python3
+"""Bench of the TwoTower denoiser-step hot path on B300.
+
+One step = one denoiser step of a block: tt_block_init (block of mask tokens),
+then block-query attention for each of the denoiser's 6 attention layers (layer
+i reads its own context-tower K/V cache), then one confidence-unmasking step
+over the block's logits.  Inputs are synthetic, seeded and resident in HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+Prints one JSON line (rank 0).  value = block-attention query tokens per second
+summed over the attention layers (B*S*layers per step / step time) over all
+ranks; the JSON also carries attention HBM GB/s against the measured roofline,
+unmask positions/s, an end-to-end figure through the C ABI with host buffers,
+and the fp64 oracle timed on the host cores on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from block_mask_diffusion_tt_b300 import synth, tt  # noqa: E402
+
+METRIC = "block-attn query-tokens/s + HBM GB/s (% roofline); unmask positions/s"
+UNIT = "query-tokens/s"
+NORTH_STAR_HBM_GBS = 8000.0
+
+
+def measured_peaks() -> dict:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return dict(hbm_gbs=float(p["hbm_gbs"]), source="measured")
+    except Exception:
+        return dict(hbm_gbs=6400.0, source="fallback")
+
+
+# ------------------------------------------------------------------ distributed plumbing
+class Dist:
+    def __init__(self, want: int, init: bool = True):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1 and init:
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            dist.init_process_group(backend)
+            self.pg = dist
+        if want != self.world and self.world > 1 and self.rank == 0:
+            print(f"warning: --gpus {want} but WORLD_SIZE {self.world}", file=sys.stderr)
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, local_rank: int):
+        self.proc = None
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        gpu_index = ids[local_rank] if local_rank < len(ids) else str(local_rank)
+        self.path = os.path.join("/tmp", f"tt_clocks_{os.getpid()}.csv")
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.out,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        top = max(power) if power else 0.0
+        loaded = [s for s, p in zip(sm, power) if p >= 0.5 * top] or sm
+        return {"sm_mhz": float(np.median(loaded)), "sm_max_mhz": float(max(smax)),
+                "reasons": sorted(reasons), "samples": len(sm), "power_w_max": top}
+
+
+# ------------------------------------------------------------------ workload on the device
+class DeviceWorkload:
+    def __init__(self, w: synth.Workload, seed: int, device: str):
+        a = w.attn
+        self.w, self.a, self.dev = w, a, device
+        g = torch.Generator(device=device)
+        g.manual_seed(1000 + seed)
+
+        def randn(shape):
+            return torch.randn(shape, generator=g, device=device, dtype=torch.float32).to(
+                torch.bfloat16)
+
+        self.lens_np = synth.ctx_lens_for(a, seed)
+        self.lens = torch.from_numpy(self.lens_np).to(device)
+        L = w.n_layers
+        self.layers = []
+        for _ in range(L):
+            self.layers.append(dict(
+                q=randn((a.B, a.S, a.Hq, a.d)), k_ctx=randn((a.B, a.Hkv, a.Lmax, a.d)),
+                v_ctx=randn((a.B, a.Hkv, a.Lmax, a.d)), k_blk=randn((a.B, a.S, a.Hkv, a.d)),
+                v_blk=randn((a.B, a.S, a.Hkv, a.d)),
+                out=torch.empty((a.B, a.S, a.Hq, a.d), dtype=torch.bfloat16, device=device)))
+        self.logits = tt.synth_logits(seed, 0, a.B, a.S, w.V, w.sigma,
+                                      synth.spike_threshold(w.spike_p), tt.TT_BF16)
+        self.tokens = torch.empty((a.B, a.S), dtype=torch.int32, device=device)
+        self.masked = torch.empty((a.B, a.S), dtype=torch.uint8, device=device)
+        self.conf = torch.empty((a.B, a.S), dtype=torch.float32, device=device)
+        self.now = torch.empty((a.B, a.S), dtype=torch.uint8, device=device)
+        self.remaining = torch.empty((a.B,), dtype=torch.int32, device=device)
+        l0 = self.layers[0]
+        self.attn_desc = tt.attn_desc(l0["q"], l0["k_ctx"], l0["v_ctx"], l0["k_blk"], l0["v_blk"],
+                                      l0["out"])
+        self.attn_ws = tt.Workspace(tt.block_attn_workspace_size(self.attn_desc), device)
+        self.unmask_desc = tt.unmask_desc(a.B, a.S, w.V, tt.TT_BF16, w.temperature, w.threshold,
+                                          w.mask_token_id)
+        self.unmask_ws = tt.Workspace(tt.confidence_unmask_workspace_size(self.unmask_desc),
+                                      device)
+        torch.cuda.synchronize()
+        self.lib = tt.load()
+        self.launches_per_step = 1 + L + 1
+
+    # algorithmic bytes of one attention launch: visible K/V, block K/V, Q, O
+    def attn_bytes(self) -> int:
+        a = self.a
+        kv = int(self.lens_np.sum()) * a.Hkv * a.d * 2 * 2
+        blk = a.B * a.S * a.Hkv * a.d * 2 * 2
+        qo = a.B * a.S * a.Hq * a.d * 2 * 2
+        return kv + blk + qo
+
+    def attn_flops(self) -> int:
+        a = self.a
+        return int(4 * a.S * a.Hq * a.d * (self.lens_np.astype(np.int64) + a.S).sum())
+
+    def unmask_bytes(self) -> int:  # every position masked at a block's first step
+        a = self.a
+        return a.B * a.S * self.w.V * 2 + a.B * a.S * (4 + 1 + 4 + 1 + 4) + a.B * 4
+
+    def step(self, stream, ev_attn=None, ev_unmask=None):
+        """Enqueues one denoiser step; optional event pairs bracket the kernels."""
+        sp = ctypes.c_void_p(stream.cuda_stream)
+        lib = self.lib
+        tt.check(lib.tt_block_init(ctypes.byref(self.unmask_desc), tt._ptr(self.tokens),
+                                   tt._ptr(self.masked), None, None, sp))
+        for i, ly in enumerate(self.layers):
+            if ev_attn is not None:
+                ev_attn[i][0].record(stream)
+            tt.check(lib.tt_block_attn(ctypes.byref(self.attn_desc), tt._ptr(ly["q"]),
+                                       tt._ptr(ly["k_ctx"]), tt._ptr(ly["v_ctx"]),
+                                       tt._ptr(self.lens), tt._ptr(ly["k_blk"]),
+                                       tt._ptr(ly["v_blk"]), tt._ptr(ly["out"]), None,
+                                       self.attn_ws.ptr, self.attn_ws.nbytes, sp))
+            if ev_attn is not None:
+                ev_attn[i][1].record(stream)
+        if ev_unmask is not None:
+            ev_unmask[0].record(stream)
+        tt.check(lib.tt_confidence_unmask(ctypes.byref(self.unmask_desc), tt._ptr(self.logits),
+                                          tt._ptr(self.tokens), tt._ptr(self.masked),
+                                          tt._ptr(self.conf), tt._ptr(self.now),
+                                          tt._ptr(self.remaining), 0, self.unmask_ws.ptr,
+                                          self.unmask_ws.nbytes, sp))
+        if ev_unmask is not None:
+            ev_unmask[1].record(stream)
+
+
+def run_ours(args, dist: Dist) -> dict:
+    w = synth.workloads()[args.workload]
+    dev = f"cuda:{dist.local}"
+    torch.cuda.set_device(dist.local)
+    stream = torch.cuda.Stream()
+    wl = DeviceWorkload(w, seed=w.seed + dist.rank, device=dev)
+    a = wl.a
+    clocks = ClockSampler(dist.local)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            wl.step(stream)
+        stream.synchronize()
+        # timed region: K steps with per-kernel events
+        ev_attn = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    for _ in wl.layers] for _ in range(args.steps)]
+        ev_unm = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        dist.barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for k in range(args.steps):
+            wl.step(stream, ev_attn[k], ev_unm[k])
+        end.record(stream)
+        torch.cuda.synchronize()
+        dist.barrier()
+    clk = clocks.stop()
+    ms = start.elapsed_time(end) / args.steps
+    ms_max = dist.max(ms)
+    attn_ms = [s.elapsed_time(e) for row in ev_attn for (s, e) in row]
+    unm_ms = [s.elapsed_time(e) for (s, e) in ev_unm]
+    attn_avg = float(np.mean(attn_ms))
+    unm_avg = float(np.mean(unm_ms))
+    peaks = measured_peaks()
+    ab = wl.attn_bytes()
+    achieved = ab / (attn_avg * 1e-3) / 1e9
+    n = dist.world
+    tokens_per_step = a.B * a.S * w.n_layers
+    res = dict(
+        metric=METRIC, value=n * tokens_per_step / (ms_max * 1e-3), unit=UNIT, n_gpus=n,
+        steps=args.steps, warmup=args.warmup, ms_per_step=ms_max, higher_is_better=True,
+        scaling="weak", vs_baseline=None, dtype="bf16",
+        data="synthetic (seeded torch normals for Q/K/V, counter-generated logits)",
+        config=dict(workload=w.name, B=a.B, S=a.S, Hq=a.Hq, Hkv=a.Hkv, d=a.d, Lmax=a.Lmax,
+                    sum_ctx_len=int(wl.lens_np.sum()), V=w.V, attn_layers=w.n_layers,
+                    temperature=w.temperature, gamma=w.threshold,
+                    step="block_init + 6 x tt_block_attn (distinct layer K/V) + tt_confidence_unmask",
+                    l2="inputs larger than L2: 6 layer caches of %.0f MB visible K/V each" %
+                       (ab / 1e6), parallelism=f"dp{n} (independent batches, no collective)"),
+        roofline=dict(bound="hbm", achieved=achieved, peak=peaks["hbm_gbs"], unit="GB/s",
+                      frac=achieved / peaks["hbm_gbs"], traffic=None,
+                      kernel="block_attn_mma_kernel<128>", peak_source=peaks["source"],
+                      algorithmic_bytes_per_launch=ab, avg_launch_ms=attn_avg),
+        attn=dict(query_tokens_per_s=a.B * a.S / (attn_avg * 1e-3), hbm_gbs=achieved,
+                  frac_of_measured=achieved / peaks["hbm_gbs"],
+                  frac_of_8tbs=achieved / NORTH_STAR_HBM_GBS,
+                  tflops=wl.attn_flops() / (attn_avg * 1e-3) / 1e12, avg_ms=attn_avg),
+        unmask=dict(positions_per_s=a.B * a.S / (unm_avg * 1e-3),
+                    hbm_gbs=wl.unmask_bytes() / (unm_avg * 1e-3) / 1e9,
+                    frac_of_measured=wl.unmask_bytes() / (unm_avg * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                    avg_ms=unm_avg),
+        gpu_launches=wl.launches_per_step * args.steps,
+        clocks=clk,
+    )
+    if not args.no_e2e:
+        res["e2e"] = run_e2e(args, wl, stream, dist)
+    del wl
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_e2e(args, wl: DeviceWorkload, stream, dist: Dist) -> dict:
+    """Same step through the C ABI with host inputs: per step the block's Q/K/V of
+    every layer, the logits and ctx_lens go host->device from pinned memory, and
+    the step's result (tokens, commit flags, confidences) comes back."""
+    host_in = []
+    for ly in wl.layers:
+        for k in ("q", "k_blk", "v_blk"):
+            host_in.append((ly[k].cpu().pin_memory(), ly[k]))
+    host_in.append((wl.logits.cpu().pin_memory(), wl.logits))
+    host_in.append((wl.lens.cpu().pin_memory(), wl.lens))
+    host_out = [(wl.tokens, torch.empty_like(wl.tokens, device="cpu").pin_memory()),
+                (wl.masked, torch.empty_like(wl.masked, device="cpu").pin_memory()),
+                (wl.conf, torch.empty_like(wl.conf, device="cpu").pin_memory())]
+    h2d = sum(h.numel() * h.element_size() for h, _ in host_in)
+    d2h = sum(h.numel() * h.element_size() for _, h in host_out)
+    steps = max(3, min(args.steps, 20))
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            for h, d in host_in:
+                d.copy_(h, non_blocking=True)
+            wl.step(stream)
+            for d, h in host_out:
+                h.copy_(d, non_blocking=True)
+        stream.synchronize()
+        dist.barrier()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(steps):
+            for h, d in host_in:
+                d.copy_(h, non_blocking=True)
+            wl.step(stream)
+            for d, h in host_out:
+                h.copy_(d, non_blocking=True)
+        end.record(stream)
+        torch.cuda.synchronize()
+        dist.barrier()
+    ms = dist.max(start.elapsed_time(end) / steps)
+    a = wl.a
+    return dict(value=dist.world * a.B * a.S * wl.w.n_layers / (ms * 1e-3), unit=UNIT,
+                h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h, ms_per_step=ms, steps=steps,
+                note="context K/V caches resident in HBM (the frozen tower's cache persists "
+                     "across steps); per-step block inputs and logits copied from pinned host "
+                     "memory, result copied back")
+
+
+# ------------------------------------------------------------------ oracle (CPU) timing
+def oracle_sample(w: synth.Workload, seqs, one_kv_head: bool = False) -> dict:
+    """Times the fp64 oracle on sequences `seqs` of the workload (one layer's attention,
+    all heads or one KV head's group, plus the unmask of the same rows).  Returns the
+    query-token-layer units processed, the seconds an equivalent step share takes
+    (attention + unmask/layers) and the threads used."""
+    import oracle
+    a = w.attn
+    lens = synth.ctx_lens_for(a, w.seed)
+    units, secs, threads = 0.0, 0.0, 0
+    for b in seqs:
+        L = int(lens[b])
+        hkv, hq = (1, a.Hq // a.Hkv) if one_kv_head else (a.Hkv, a.Hq)
+        shape = synth.AttnShape(1, a.S, hq, hkv, a.d, max(L, 1), lens=[L])
+        inp = synth.attn_inputs(shape, seed=w.seed + 17 * b)
+        logits = synth.counter_logits(w.seed, 0, 1, a.S, w.V, w.sigma, w.spike_p, "bf16")
+        t0 = time.perf_counter()
+        _, _, used = oracle.block_attn(inp["q"], inp["k_ctx"], inp["v_ctx"], inp["ctx_lens"],
+                                       inp["k_blk"], inp["v_blk"], return_threads=True)
+        t1 = time.perf_counter()
+        r = oracle.confidence_unmask(logits, "bf16", w.temperature, w.threshold, w.mask_token_id,
+                                     np.full((1, a.S), w.mask_token_id, np.int32),
+                                     np.ones((1, a.S), np.uint8))
+        t2 = time.perf_counter()
+        frac = hq / a.Hq
+        units += a.S * frac
+        secs += (t1 - t0) + (t2 - t1) * frac / w.n_layers
+        threads = max(threads, used, r["threads"])
+    return dict(units=units, secs=secs, threads=threads)
+
+
+def cpu_baseline(w: synth.Workload, budget_s: float) -> dict:
+    a = w.attn
+    order = list(range(a.B))
+    done, acc_units, acc_secs, threads = [], 0.0, 0.0, 0
+    t_start = time.perf_counter()
+    for b in order:
+        r = oracle_sample(w, [b])
+        done.append(b)
+        acc_units += r["units"]
+        acc_secs += r["secs"]
+        threads = max(threads, r["threads"])
+        if time.perf_counter() - t_start > budget_s:
+            break
+    lens = synth.ctx_lens_for(a, w.seed)
+    return dict(value=acc_units / acc_secs, unit=UNIT, cores=threads, kind="oracle",
+                sample=f"fp64 oracle, sequences {done} (ctx lens {[int(lens[b]) for b in done]}) "
+                       f"of one attention layer, all heads, plus their unmask rows weighted 1/"
+                       f"{w.n_layers}; {acc_secs:.1f} s of CPU work")
+
+
+def run_reference(args, dist: Dist) -> dict:
+    """The oracle as the reference arm: each step a bounded sample of the workload."""
+    w = synth.workloads()[args.workload]
+    a = w.attn
+    budget = 150.0  # seconds for the whole run
+    probe = oracle_sample(w, [0])
+    per_step = probe["secs"]
+    one_kv = per_step * (args.steps + args.warmup) > budget
+    units, secs, threads = 0.0, 0.0, probe["threads"]
+    seq = 1
+    for _ in range(max(0, args.warmup - 1)):
+        oracle_sample(w, [seq % a.B], one_kv)
+        seq += 1
+    for _ in range(args.steps):
+        r = oracle_sample(w, [seq % a.B], one_kv)
+        seq += 1
+        units += r["units"]
+        secs += r["secs"]
+        threads = max(threads, r["threads"])
+    value = units / secs
+    sample = ("fp64 oracle on the host cores; each step one sequence of the workload (cycling), "
+              + ("one KV head's query group" if one_kv else "all heads")
+              + f", one attention layer plus its unmask rows weighted 1/{w.n_layers}")
+    return dict(
+        impl="reference", metric=METRIC, value=value, unit=UNIT, n_gpus=dist.world,
+        steps=args.steps, warmup=args.warmup, ms_per_step=1e3 * secs / max(args.steps, 1),
+        higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64",
+        data="synthetic (numpy PCG64 normals, counter-generated logits)",
+        config=dict(workload=w.name, B=a.B, S=a.S, Hq=a.Hq, Hkv=a.Hkv, d=a.d, Lmax=a.Lmax,
+                    V=w.V, attn_layers=w.n_layers),
+        cpu_baseline=dict(kind="oracle", cores=threads, sample=sample, value=value, unit=UNIT),
+        e2e=dict(value=value, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0),
+        gpu_launches=0)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="ragged16k", choices=sorted(synth.workloads()))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    dist = Dist(args.gpus, init=args.impl == "ours")
+    try:
+        if args.impl == "reference":
+            if dist.rank == 0:
+                print(json.dumps(run_reference(args, dist)), flush=True)
+            return
+        res = run_ours(args, dist)
+        if dist.rank == 0:
+            if dist.world == 1:
+                res["cpu_baseline"] = cpu_baseline(synth.workloads()[args.workload],
+                                                   args.cpu_budget_s)
+            print(json.dumps(res), flush=True)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -328,7 +328,7 @@ __global__ void block_init_kernel(int n, int S, int mask_id, int32_t *tokens, ui
     tokens[i] = mask_id;
     is_masked[i] = 1;
     if (committed_step) committed_step[i] = -1;
-    if (i % S == 0) steps_used[i / S] = 0;
+    if (steps_used && i % S == 0) steps_used[i / S] = 0;
 }
 
 __global__ void count_masked_kernel(int B, int S, const uint8_t *is_masked, int32_t *remaining) {
@@ -494,6 +494,20 @@ tt_status tt_confidence_unmask(const tt_unmask_desc *d, const void *logits, int3
         return fail(TT_ERR_WORKSPACE, "%s: workspace not 256-byte aligned", fn);
     return launch_unmask(d, logits, tokens, is_masked, conf, committed_now, remaining,
                          force_commit_all, w, 0, nullptr, nullptr, (cudaStream_t)stream);
+}
+
+tt_status tt_block_init(const tt_unmask_desc *d, int32_t *tokens, uint8_t *is_masked,
+                        int32_t *steps_used, int32_t *committed_step, tt_stream_t stream) {
+    const char *fn = "tt_block_init";
+    if (!d) return fail(TT_ERR_INVALID_ARG, "%s: null desc", fn);
+    if (d->B < 0 || d->S < 1) return fail(TT_ERR_INVALID_ARG, "%s: bad B or S", fn);
+    if (d->B == 0) return TT_OK;
+    if (!tokens || !is_masked) return fail(TT_ERR_INVALID_ARG, "%s: null pointer", fn);
+    const int64_t n = static_cast<int64_t>(d->B) * d->S;
+    if (n > 2147483647LL) return fail(TT_ERR_UNSUPPORTED, "%s: B*S too large", fn);
+    block_init_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, (cudaStream_t)stream>>>(
+        static_cast<int>(n), d->S, d->mask_token_id, tokens, is_masked, steps_used, committed_step);
+    return cuda_status(cudaGetLastError(), fn);
 }
 
 size_t tt_denoise_block_loop_workspace_size(const tt_unmask_desc *d) {

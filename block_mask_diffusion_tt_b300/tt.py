@@ -77,6 +77,7 @@ def load(path: str = LIB_PATH):
         "tt_confidence_unmask_workspace_size": (_sz, [ctypes.POINTER(UnmaskDesc)]),
         "tt_confidence_unmask": (ctypes.c_int, [ctypes.POINTER(UnmaskDesc), _p, _p, _p, _p, _p, _p,
                                                 _i32, _p, _sz, _p]),
+        "tt_block_init": (ctypes.c_int, [ctypes.POINTER(UnmaskDesc), _p, _p, _p, _p, _p]),
         "tt_denoise_block_loop_workspace_size": (_sz, [ctypes.POINTER(UnmaskDesc)]),
         "tt_denoise_block_loop": (ctypes.c_int, [ctypes.POINTER(UnmaskDesc), _i32, _i32, _i32, _p,
                                                  _p, _p, _p, _p, _p, _p, _p, _sz, _p, _i32,
@@ -261,6 +262,17 @@ def synth_params(seed: int, B: int, S: int, V: int, dtype: int, sigma: float,
     return p
 
 
+def block_init(tokens, is_masked, mask_token_id: int, steps_used=None, committed_step=None,
+               stream=None):
+    """Starts a block on the device (tt_block_init): all positions masked."""
+    _need(tokens, "tokens", torch.int32, 2)
+    _need(is_masked, "is_masked", torch.uint8, 2)
+    B, S = tokens.shape
+    desc = unmask_desc(B, S, 1, TT_F32, 1.0, 0.0, mask_token_id)
+    check(load().tt_block_init(ctypes.byref(desc), _ptr(tokens), _ptr(is_masked), _ptr(steps_used),
+                               _ptr(committed_step), _stream(stream)))
+
+
 def denoise_block_loop_workspace_size(desc: UnmaskDesc) -> int:
     return int(load().tt_denoise_block_loop_workspace_size(ctypes.byref(desc)))
 
@@ -316,5 +328,6 @@ def exported_symbols() -> list:
     """Names of the entry points this binding expects libtt.so to export."""
     return ["tt_status_string", "tt_last_error", "tt_abi_version", "tt_workspace_zero",
             "tt_block_attn_workspace_size", "tt_block_attn", "tt_confidence_unmask_workspace_size",
-            "tt_confidence_unmask", "tt_denoise_block_loop_workspace_size", "tt_denoise_block_loop",
+            "tt_confidence_unmask", "tt_block_init", "tt_denoise_block_loop_workspace_size",
+            "tt_denoise_block_loop",
             "tt_synth_logits", "tt_synth_logits_producer"]

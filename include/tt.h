@@ -205,6 +205,14 @@ typedef tt_status (*tt_logits_fn)(void *user, int32_t step, const int32_t *token
                                   const uint8_t *is_masked, void *logits_out,
                                   tt_stream_t stream);
 
+/*
+ * Starts a block: tokens[b,s] = mask_token_id and is_masked[b,s] = 1 for every
+ * position; steps_used[b] = 0 and committed_step[b,s] = -1 when those (device,
+ * nullable) are given.  Uses desc's B, S and mask_token_id only.
+ */
+tt_status tt_block_init(const tt_unmask_desc *desc, int32_t *tokens, uint8_t *is_masked,
+                        int32_t *steps_used, int32_t *committed_step, tt_stream_t stream);
+
 /* Bytes of device workspace tt_denoise_block_loop needs (0 on invalid desc). */
 size_t tt_denoise_block_loop_workspace_size(const tt_unmask_desc *desc);
 
