@@ -23,6 +23,8 @@
 // through a 3-stage cp.async ring with zero fill for keys past the prefix.
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace tt {
@@ -593,3 +595,124 @@ tt_status tt_block_attn(const tt_attn_desc *d, const void *q, const void *k_ctx,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- no-allocation variant
+// Scratch of tt_block_attn_noalloc: a fixed device array in this module, present
+// on every device that loads the library for as long as the process lives.
+namespace tt {
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(32) << 20;  // 32 MiB per device
+static __device__ __align__(256) unsigned char g_attn_static_scratch[kStaticScratchBytes];
+
+std::mutex g_static_mu;
+void *g_static_ptr[64] = {nullptr};  // device address of the array, per device
+
+// Device address of the static scratch on the current device.  The first call on
+// a device resolves it with cudaGetSymbolAddress (the array's name is only a host
+// stand-in in host code).
+tt_status static_scratch(void **out, const char *fn) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e, fn);
+    if (dev < 0 || dev >= 64) return fail(TT_ERR_UNSUPPORTED, "%s: device index %d >= 64", fn, dev);
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_attn_static_scratch);
+        if (e != cudaSuccess) return cuda_status(e, "cudaGetSymbolAddress(static scratch)");
+        g_static_ptr[dev] = p;
+    }
+    *out = g_static_ptr[dev];
+    return TT_OK;
+}
+
+// Layout of the static scratch for `slots` partial slots.
+AttnWs carve_static(void *base, int npairs, size_t slots, int d) {
+    Carve c(base);
+    AttnWs w;
+    w.pair_cnt = c.take<unsigned>(static_cast<size_t>(npairs));
+    w.part_ml = c.take<float2>(slots * kRows);
+    w.part_o = c.take<float>(slots * kRows * d);
+    w.bytes = c.bytes();
+    return w;
+}
+
+}  // namespace
+}  // namespace tt
+
+extern "C" tt_status tt_block_attn_noalloc(const tt_attn_desc *d, const void *q,
+                                           const void *k_ctx, const void *v_ctx,
+                                           const int32_t *ctx_lens, const void *k_blk,
+                                           const void *v_blk, void *out, float *lse,
+                                           tt_stream_t stream) {
+    using namespace tt;
+    const char *fn = "tt_block_attn_noalloc";
+    Geometry g;
+    tt_status st = validate(d, &g, fn);
+    if (st != TT_OK) return st;
+    if (d->B == 0) return TT_OK;
+    if (!q || !k_blk || !v_blk || !out || !ctx_lens || (d->Lmax > 0 && (!k_ctx || !v_ctx)))
+        return fail(TT_ERR_INVALID_ARG, "%s: null pointer", fn);
+    const void *ptrs[6] = {q, k_ctx, v_ctx, k_blk, v_blk, out};
+    for (int i = 0; i < 6; ++i)
+        if (reinterpret_cast<uintptr_t>(ptrs[i]) % 16)
+            return fail(TT_ERR_INVALID_ARG, "%s: tensor base not 16-byte aligned", fn);
+    if (reinterpret_cast<uintptr_t>(ctx_lens) % 4 || (lse && reinterpret_cast<uintptr_t>(lse) % 4))
+        return fail(TT_ERR_INVALID_ARG, "%s: ctx_lens/lse misaligned", fn);
+    // slots that fit: one per pair plus at least one partition
+    const size_t per_slot = carve_static(nullptr, 0, 1, d->d).bytes;
+    size_t slots = kStaticScratchBytes / per_slot;
+    while (slots > 0 && carve_static(nullptr, g.npairs, slots, d->d).bytes > kStaticScratchBytes)
+        --slots;
+    if (slots < static_cast<size_t>(g.npairs) + 1)
+        return fail(TT_ERR_UNSUPPORTED,
+                    "%s: B*Hkv*ceil(S*Hq/Hkv/256) = %d pairs need more than the %zu-byte static "
+                    "scratch (at most %zu pairs at d=%d); use tt_block_attn with a workspace",
+                    fn, g.npairs, kStaticScratchBytes, slots > 0 ? slots - 1 : 0, d->d);
+    const size_t parts = slots - g.npairs;
+    if (static_cast<size_t>(g.P) > parts) g.P = static_cast<int>(parts);
+    void *base = nullptr;
+    if ((st = static_scratch(&base, fn)) != TT_OK) return st;
+    AttnWs w = carve_static(base, g.npairs, static_cast<size_t>(g.P) + g.npairs, d->d);
+    // the arrival counters must start at zero whatever an earlier call left behind
+    st = cuda_status(cudaMemsetAsync(w.pair_cnt, 0, sizeof(unsigned) * g.npairs,
+                                     (cudaStream_t)stream), fn);
+    if (st != TT_OK) return st;
+
+    AttnArgs a;
+    a.q = static_cast<const uint16_t *>(q);
+    a.kctx = static_cast<const uint16_t *>(k_ctx ? k_ctx : q);
+    a.vctx = static_cast<const uint16_t *>(v_ctx ? v_ctx : q);
+    a.kblk = static_cast<const uint16_t *>(k_blk);
+    a.vblk = static_cast<const uint16_t *>(v_blk);
+    a.out = static_cast<uint16_t *>(out);
+    a.lse = lse;
+    for (int i = 0; i < 4; ++i) {
+        a.qs[i] = d->q_strides[i];
+        a.kcs[i] = d->kctx_strides[i];
+        a.vcs[i] = d->vctx_strides[i];
+        a.kbs[i] = d->kblk_strides[i];
+        a.vbs[i] = d->vblk_strides[i];
+        a.os[i] = d->o_strides[i];
+    }
+    a.lens = ctx_lens;
+    a.B = d->B;
+    a.S = d->S;
+    a.Hq = d->Hq;
+    a.Hkv = d->Hkv;
+    a.G = g.G;
+    a.Lmax = d->Lmax;
+    a.R = g.R;
+    a.NRG = g.NRG;
+    a.npairs = g.npairs;
+    a.P = g.P;
+    const double scale = d->scale > 0.f ? d->scale : 1.0 / sqrt(static_cast<double>(d->d));
+    a.scale_log2 = static_cast<float>(scale * 1.4426950408889634);
+    a.part_o = w.part_o;
+    a.part_ml = w.part_ml;
+    a.pair_cnt = w.pair_cnt;
+    const int extra = (g.npairs + 1) * static_cast<int>(sizeof(int));
+    if (d->d == 128) return launch<128>(a, Layout<128>::kBytes + extra, (cudaStream_t)stream);
+    return launch<64>(a, Layout<64>::kBytes + extra, (cudaStream_t)stream);
+}

@@ -187,6 +187,25 @@ def block_attn(q, k_ctx, v_ctx, ctx_lens, k_blk, v_blk, out=None, lse=None, scal
     return out
 
 
+def block_attn_noalloc(q, k_ctx, v_ctx, ctx_lens, k_blk, v_blk, out=None, lse=None,
+                      scale: float = 0.0, stream=None):
+    """tt_block_attn_noalloc: block attention with the library's fixed scratch.
+
+    For callers that cannot allocate device memory: no workspace argument, and no
+    allocation inside the call.  Calls must not overlap on the GPU.
+    """
+    lib = load()
+    fn = lib.tt_block_attn_noalloc
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.POINTER(AttnDesc), _p, _p, _p, _p, _p, _p, _p, _p, _p]
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    desc = attn_desc(q, k_ctx, v_ctx, k_blk, v_blk, out, scale)
+    check(fn(ctypes.byref(desc), _ptr(q), _ptr(k_ctx), _ptr(v_ctx), _ptr(ctx_lens), _ptr(k_blk),
+             _ptr(v_blk), _ptr(out), _ptr(lse), _stream(stream)))
+    return out
+
+
 # ------------------------------------------------------------------ unmasking
 def unmask_desc(B, S, V, dtype, temperature, threshold, mask_token_id, row_stride=0) -> UnmaskDesc:
     return UnmaskDesc(B=B, S=S, V=V, logits_dtype=dtype, logits_row_stride=row_stride,
@@ -327,7 +346,8 @@ def denoise_block_loop(B: int, S: int, V: int, logits_dtype: int, temperature: f
 def exported_symbols() -> list:
     """Names of the entry points this binding expects libtt.so to export."""
     return ["tt_status_string", "tt_last_error", "tt_abi_version", "tt_workspace_zero",
-            "tt_block_attn_workspace_size", "tt_block_attn", "tt_confidence_unmask_workspace_size",
+            "tt_block_attn_workspace_size", "tt_block_attn", "tt_block_attn_noalloc",
+            "tt_confidence_unmask_workspace_size",
             "tt_confidence_unmask", "tt_block_init", "tt_denoise_block_loop_workspace_size",
             "tt_denoise_block_loop",
             "tt_synth_logits", "tt_synth_logits_producer"]

@@ -144,6 +144,32 @@ tt_status tt_block_attn(const tt_attn_desc *desc, const void *q, const void *k_c
                         const void *v_blk, void *out, float *lse, void *workspace,
                         size_t workspace_bytes, tt_stream_t stream);
 
+/*
+ * tt_block_attn without a caller-provided workspace.  The TwoTower pages have
+ * no counterpart to this entry point: it exists for callers that cannot
+ * allocate device memory, such as code embedded in a host program whose device
+ * memory all belongs to another allocator's pool, or a latency-critical loop
+ * that must never call cudaMalloc because it can synchronize the device.
+ * Same arguments and result as tt_block_attn, minus the workspace.
+ *  - Scratch is a fixed 32 MiB device array inside libtt (file-scope static);
+ *    every GPU that loads the library holds it until the process exits.  No
+ *    call allocates or frees memory.
+ *  - Limit: B*Hkv*ceil(S*(Hq/Hkv)/256) "pairs" must leave room for at least one
+ *    partial slot per pair plus one: at d=128 about 250 pairs (e.g. B=125 with
+ *    Hkv=2), at d=64 about 500.  Larger shapes return TT_ERR_UNSUPPORTED with a
+ *    message; when the scratch holds fewer partial slots than the device has
+ *    SMs the prefix is split across fewer SMs (same result up to fp32 rounding).
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress); make that first call before any stream capture.
+ *  - Every call shares the one array and clears its arrival counters on
+ *    `stream` before the kernel: calls that overlap on the GPU (other streams,
+ *    other host threads without ordering) race and corrupt each other's
+ *    results.  Order them on one stream.
+ */
+tt_status tt_block_attn_noalloc(const tt_attn_desc *desc, const void *q, const void *k_ctx,
+                                const void *v_ctx, const int32_t *ctx_lens, const void *k_blk,
+                                const void *v_blk, void *out, float *lse, tt_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Confidence unmasking                                                      */
 /* ------------------------------------------------------------------------ */
