@@ -1,4 +1,5 @@
-// attn.cu -- block-query attention of one denoiser attention layer.
+// attn.cu -- block-query attention of one denoiser attention layer on sm_103a
+// (tcgen05 tensor cores with TMEM accumulators, TMA-staged K/V).
 //
 // Method (dothoosh.com "فرآیند انتشار در برابر رمزگشایی متوالی در مدل جدید انویدیا",
 // section "two-tower mechanism"; aitrends.kr "Nemotron-Labs-TwoTower-30B-A3B-Base-BF16",
@@ -7,20 +8,34 @@
 // followed by the block's own S keys; every block query sees every block key.
 // Grouped-query heads: query head h reads KV head h / (Hq/Hkv).
 //
-// Work decomposition (all on the device, from ctx_lens):
+// Work decomposition (on the device, from ctx_lens):
 //  * a "pair" is (sequence b, KV head g, row group rg): the R = S*Hq/Hkv query
 //    rows (s, h in group g) that share one K/V stream, cut into groups of 256;
+//    each group runs as two 128-row halves (one tcgen05 M=128 tile each);
 //  * pair p owns ceil(L_b/64) context tiles of 64 keys plus one block tile;
-//  * all tiles of all pairs are laid end to end and cut into P equal ranges, one
-//    per CTA (P = min(#SMs, tiles/kMinTiles)); a CTA walks its range pair by pair;
-//  * a pair whose tiles fall in one CTA is finished in registers; otherwise each
-//    CTA writes an fp32 partial (O, running max m, sum l) and the last CTA to
-//    arrive (per-pair counter) merges them: M = max m_c,
+//  * the tiles of all pairs are laid end to end and cut into P equal ranges, one
+//    per CTA (P = min(#SMs, tiles/4)); a CTA walks its range segment by segment
+//    (a segment = the part of one pair inside the range);
+//  * a pair whose tiles fall in one CTA is finished there; otherwise each CTA
+//    writes an fp32 partial (O, running max m, sum l) and the last CTA to arrive
+//    (per pair and half) merges them: M = max m_c,
 //    O = sum 2^(m_c-M) O_c / sum 2^(m_c-M) l_c.  No CTA waits on another.
 //
-// Per tile: Q K^T and P V on the tensor cores (bf16 mma.sync m16n8k16, fp32
-// accumulate), online softmax in the exp2 domain, K/V staged in shared memory
-// through a 3-stage cp.async ring with zero fill for keys past the prefix.
+// Inside a CTA (320 threads, one CTA per SM, 512 TMEM columns):
+//  warp 8     TMA producer: K and V tiles (64 keys x d, 128-byte swizzle) into a
+//             ring of shared-memory stages (full/empty mbarriers);
+//  warp 9     MMA issuer: S_h = Q_h K^T (A = Q_h in TMEM, B = K tile in smem,
+//             M=128 N=64), then O_h += P_h V (A = P_h in TMEM, B = V tile read
+//             MN-major, M=128 N=d); completion via tcgen05.commit;
+//  warps 0-7  softmax, warpgroup h owns half h, one query row per thread: reads
+//             its S row from TMEM, keeps the running max (in log2 units, raised
+//             only when it grows by more than 8, so O is rescaled rarely) and
+//             sum, writes P = 2^(x - m) as bf16 over the S columns, and at the
+//             end of a segment reads O, normalises and stores it.
+// TMEM columns (d=128): Q_0 Q_1 [64 each] | S_0 S_1 [64 each] | O_0 O_1 [128 each].
+// Every wait on an mbarrier gives up after 2 s (globaltimer), records a flag in
+// the workspace and lets the CTA drain its copies and free TMEM.
+#include <cuda.h>
 #include <math.h>
 
 #include <mutex>
@@ -30,205 +45,596 @@
 namespace tt {
 namespace {
 
-constexpr int kRows = 256;   // query rows per pair
-constexpr int kWarps = 16;   // 16 rows per warp
-constexpr int kThreads = kWarps * 32;
-constexpr int kTN = 64;      // keys per tile
-constexpr int kStages = 3;
+constexpr int kRows = 256;  // query rows per pair (two halves of 128)
+constexpr int kTN = 64;     // keys per tile
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
 constexpr int kMaxPairs = 4096;
 constexpr int kMinTiles = 4;  // smallest tile range worth a partial
 constexpr float kLn2 = 0.69314718055994531f;
+constexpr float kRescaleLog2 = 8.f;  // lazy rescale: O is rescaled when the max grows by > 2^8
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr int kTmemCols = 512;
+
+template <int D>
+struct Cfg {
+    static constexpr int kChunks = D / 64;            // 64-column (128-byte) chunks of a row
+    static constexpr int kRegionBytes = kTN * 128;    // one chunk of a 64-key tile
+    static constexpr int kStageBytes = 2 * kChunks * kRegionBytes;  // K chunks then V chunks
+    static constexpr int kStages = D == 128 ? 5 : 8;
+    static constexpr int kQCols = D / 2;  // bf16 pairs per row
+    __host__ __device__ static constexpr uint32_t colQ(int h) { return h * kQCols; }
+    __host__ __device__ static constexpr uint32_t colS(int h) { return 2 * kQCols + h * kTN; }
+    __host__ __device__ static constexpr uint32_t colO(int h) { return 2 * kQCols + 2 * kTN + h * D; }
+    // instruction descriptors (kind::f16): D fp32, A/B bf16, M=128
+    static constexpr uint32_t kIdescQK = (1u << 4) | (1u << 7) | (1u << 10) |
+                                         (uint32_t(kTN >> 3) << 17) | (uint32_t(128 >> 4) << 24);
+    static constexpr uint32_t kIdescPV = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
+                                         (uint32_t(D >> 3) << 17) | (uint32_t(128 >> 4) << 24);
+    // barriers: full[S] empty[S] s_full[2] p_full[2] pv_done[2] q_ready[2] wg_bar[2] fin
+    static constexpr int kNumBars = 2 * kStages + 11;
+    static constexpr int kBarOffset = kStages * kStageBytes;
+    static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;  // tmem base, err, last[2]
+    static constexpr int kPrefixOffset = kMiscOffset + 16;
+    static constexpr int smem_bytes(int npairs) { return 1024 + kPrefixOffset + (npairs + 1) * 4; }
+    static_assert(2 * kQCols + 2 * kTN + 2 * D <= kTmemCols, "TMEM budget");
+};
 
 struct AttnArgs {
-    const uint16_t *q, *kctx, *vctx, *kblk, *vblk;
+    const uint16_t *q;
     uint16_t *out;
     float *lse;
-    int64_t qs[4], kcs[4], vcs[4], kbs[4], vbs[4], os[4];
+    int64_t qs[4], os[4];
     const int32_t *lens;
     int B, S, Hq, Hkv, G, Lmax, R, NRG, npairs, P;
     float scale_log2;
-    float *part_o;    // [slots][256][D]
+    float *part_o;    // [slots][D][256]
     float2 *part_ml;  // [slots][256]
-    unsigned *pair_cnt;
+    unsigned *pair_cnt;  // [npairs][2]
+    int *err_word;
 };
 
+// ---------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
-    const int n = valid ? 16 : 0;
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n));
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
-}
-
-__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
     asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};\n"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
 }
 
-// CTA (of P) whose tile range holds flattened tile t, T tiles in total.
+// Waits for the phase of `parity` to complete.  Gives up (false) when another
+// role has flagged an error or after kWaitLimitNs, flagging `code`.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *err,
+                                       int code) {
+    if (mbar_try(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try(bar, parity)) return true;
+        if ((i & 63) == 0) {
+            if (*err) return false;
+            if (globaltimer() - t0 > kWaitLimitNs) {
+                atomicCAS(const_cast<int *>(err), 0, code);
+                return false;
+            }
+        }
+    }
+}
+// Bounded wait that ignores the error flag (used to drain copies in flight).
+__device__ __noinline__ bool mbar_drain(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try(bar, parity))
+        if (globaltimer() - t0 > kWaitLimitNs) return false;
+    return true;
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, int c3, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     bar)
+                 : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem desc]
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Shared-memory matrix descriptor, 128-byte swizzle (sm_100 format, version 1).
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    return uint64_t((addr & 0x3FFFFu) >> 4) | (uint64_t(lbo >> 4) << 16) |
+           (uint64_t(sbo >> 4) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
+#define TT_R32(r)                                                                              \
+    "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),       \
+        "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), \
+        "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),          \
+        "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),          \
+        "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+#define TT_W32(r)                                                                              \
+    "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),       \
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), \
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),          \
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),          \
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+#define TT_IN32(r)                                                                             \
+    "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),   \
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),      \
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),    \
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),    \
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+#define TT_REGLIST32                                                                           \
+    "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, "   \
+    "%19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}"
+
+// 32 consecutive 32-bit TMEM columns of this thread's lane (shape 32x32b).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t *r) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 " TT_REGLIST32 ", [%32];"
+                 : TT_W32(r)
+                 : "r"(taddr));
+}
+// Completes the loads; the registers pass through so no use moves above the wait.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t *r) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : TT_R32(r)::"memory");
+}
+__device__ __forceinline__ void tmem_touch(uint32_t *r) { asm volatile("" : TT_R32(r)); }
+#define TT_REGLIST32_FROM1                                                                     \
+    "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, "  \
+    "%20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32}"
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], " TT_REGLIST32_FROM1 ";" ::"r"(
+                     taddr),
+                 TT_IN32(r)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- scheduling
+struct Seg {
+    int p, b, g, rg, L, nctx, rows, nh, tile0, ntiles, c_first, c_last;
+};
+
 __device__ __forceinline__ int owner_of(int64_t t, int P, int64_t T) {
     return static_cast<int>(((t + 1) * P - 1) / T);
 }
 
-struct PairInfo {
-    int b, g, rg, L, nctx_tiles, rows;
-};
+struct Sched {
+    const int *prefix;
+    int P;
+    int64_t T, tcur, tend;
 
-__device__ __forceinline__ PairInfo pair_info(const AttnArgs &a, int p) {
-    PairInfo pi;
-    pi.rg = p % a.NRG;
-    const int bg = p / a.NRG;
-    pi.g = bg % a.Hkv;
-    pi.b = bg / a.Hkv;
-    int L = a.lens[pi.b];
-    pi.L = L < 0 ? 0 : (L > a.Lmax ? a.Lmax : L);
-    pi.nctx_tiles = (pi.L + kTN - 1) / kTN;
-    pi.rows = min(kRows, a.R - pi.rg * kRows);
-    return pi;
-}
-
-template <int D>
-struct Layout {
-    static constexpr int kStride = D + 8;  // bf16 elements per smem row (conflict-free ldmatrix)
-    static constexpr int kQBytes = kRows * kStride * 2;
-    static constexpr int kTileBytes = kTN * kStride * 2;
-    static constexpr int kStageBytes = 2 * kTileBytes;  // K then V
-    static constexpr int kBytes = kQBytes + kStages * kStageBytes;
-};
-
-// Enqueues the cp.async copies of tile `tile` of pair `pi` into stage memory.
-template <int D>
-__device__ __forceinline__ void load_tile(const AttnArgs &a, const PairInfo &pi, int tile,
-                                          uint16_t *ks, uint16_t *vs) {
-    constexpr int kChunks = D / 8;  // 16-byte chunks per row
-    const bool block_tile = tile == pi.nctx_tiles;
-    const int nvalid = block_tile ? a.S : min(kTN, pi.L - tile * kTN);
-    for (int i = threadIdx.x; i < kTN * kChunks; i += kThreads) {
-        const int j = i / kChunks, ch = i % kChunks;
-        const bool valid = j < nvalid;
-        const uint16_t *ksrc, *vsrc;
-        if (block_tile) {
-            const int jj = valid ? j : 0;
-            ksrc = a.kblk + pi.b * a.kbs[0] + jj * a.kbs[1] + pi.g * a.kbs[2] + ch * 8;
-            vsrc = a.vblk + pi.b * a.vbs[0] + jj * a.vbs[1] + pi.g * a.vbs[2] + ch * 8;
-        } else {
-            const int64_t key = valid ? static_cast<int64_t>(tile) * kTN + j : 0;
-            ksrc = a.kctx + pi.b * a.kcs[0] + pi.g * a.kcs[1] + key * a.kcs[2] + ch * 8;
-            vsrc = a.vctx + pi.b * a.vcs[0] + pi.g * a.vcs[1] + key * a.vcs[2] + ch * 8;
+    __device__ bool next(const AttnArgs &a, Seg &s) {
+        if (tcur >= tend) return false;
+        int lo = 0, hi = a.npairs;  // prefix[lo] <= tcur < prefix[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (prefix[mid] <= tcur) lo = mid; else hi = mid;
         }
-        const int off = j * Layout<D>::kStride + ch * 8;
-        cp_async16(smem_u32(ks + off), ksrc, valid);
-        cp_async16(smem_u32(vs + off), vsrc, valid);
+        const int p = lo;
+        const int64_t ps = prefix[p], pe = prefix[p + 1];
+        const int64_t seg_end = pe < tend ? pe : tend;
+        s.p = p;
+        s.rg = p % a.NRG;
+        const int bg = p / a.NRG;
+        s.g = bg % a.Hkv;
+        s.b = bg / a.Hkv;
+        int L = a.lens[s.b];
+        s.L = L < 0 ? 0 : (L > a.Lmax ? a.Lmax : L);
+        s.nctx = (s.L + kTN - 1) / kTN;
+        s.rows = min(kRows, a.R - s.rg * kRows);
+        s.nh = s.rows > 128 ? 2 : 1;
+        s.tile0 = static_cast<int>(tcur - ps);
+        s.ntiles = static_cast<int>(seg_end - tcur);
+        s.c_first = owner_of(ps, P, T);
+        s.c_last = owner_of(pe - 1, P, T);
+        tcur = seg_end;
+        return true;
     }
+};
+
+__device__ __forceinline__ int tile_valid(const AttnArgs &a, const Seg &s, int tile) {
+    return tile == s.nctx ? a.S : min(kTN, s.L - tile * kTN);
 }
 
+// ---------------------------------------------------------------- roles
 template <int D>
-__device__ __forceinline__ void load_q(const AttnArgs &a, const PairInfo &pi, uint16_t *qs) {
-    constexpr int kChunks = D / 8;
-    for (int i = threadIdx.x; i < kRows * kChunks; i += kThreads) {
-        const int r = i / kChunks, ch = i % kChunks;
-        const bool valid = r < pi.rows;
-        const int rr = pi.rg * kRows + (valid ? r : 0);
-        const int s = rr / a.G, h = pi.g * a.G + rr % a.G;
-        const uint16_t *src = a.q + pi.b * a.qs[0] + s * a.qs[1] + h * a.qs[2] + ch * 8;
-        cp_async16(smem_u32(qs + r * Layout<D>::kStride + ch * 8), src, valid);
-    }
-}
+struct Smem {
+    uint32_t stages, bars;
+    int *prefix;
+    volatile int *err;
+    volatile int *last;
+    uint32_t *tmem_slot;
+    __device__ uint32_t full(int i) const { return bars + 8 * i; }
+    __device__ uint32_t empty(int i) const { return bars + 8 * (Cfg<D>::kStages + i); }
+    __device__ uint32_t s_full(int h) const { return bars + 8 * (2 * Cfg<D>::kStages + h); }
+    __device__ uint32_t p_full(int h) const { return bars + 8 * (2 * Cfg<D>::kStages + 2 + h); }
+    __device__ uint32_t pv_done(int h) const { return bars + 8 * (2 * Cfg<D>::kStages + 4 + h); }
+    __device__ uint32_t q_ready(int h) const { return bars + 8 * (2 * Cfg<D>::kStages + 6 + h); }
+    __device__ uint32_t wg_bar(int h) const { return bars + 8 * (2 * Cfg<D>::kStages + 8 + h); }
+    __device__ uint32_t fin() const { return bars + 8 * (2 * Cfg<D>::kStages + 10); }
+};
 
-// Writes one finished row pair (rows g and g+8 of the warp) for a single-part pair.
 template <int D>
-__device__ __forceinline__ void store_rows(const AttnArgs &a, const PairInfo &pi, int row,
-                                           const float (&o)[D / 8][4], int half, float inv_l,
-                                           float m, float l) {
-    if (row >= pi.rows) return;
-    const int rr = pi.rg * kRows + row;
-    const int s = rr / a.G, h = pi.g * a.G + rr % a.G;
-    const int c = threadIdx.x & 3;
-    uint16_t *dst = a.out + pi.b * a.os[0] + s * a.os[1] + h * a.os[2];
+__device__ void role_producer(const AttnArgs &a, Sched sch, const Smem<D> &sm,
+                              const CUtensorMap *tkc, const CUtensorMap *tvc,
+                              const CUtensorMap *tkb, const CUtensorMap *tvb) {
+    using C = Cfg<D>;
+    int stage = 0;
+    uint32_t phase = 0, issued = 0, last_par = 0;
+    Seg s;
+    bool ok = true;
+    while (ok && sch.next(a, s)) {
+        for (int it = 0; it < s.ntiles; ++it) {
+            if (!mbar_wait(sm.empty(stage), phase ^ 1, sm.err, 1)) { ok = false; break; }
+            const uint32_t full = sm.full(stage);
+            mbar_expect_tx(full, C::kStageBytes);
+            const int tile = s.tile0 + it;
+            const bool blk = tile == s.nctx;
+            // ctx maps: (d, Lmax, Hkv, B); block maps: (d, Hkv, S, B)
+            const CUtensorMap *mk = blk ? tkb : tkc;
+            const CUtensorMap *mv = blk ? tvb : tvc;
+            const int c1 = blk ? s.g : tile * kTN, c2 = blk ? 0 : s.g;
+            const uint32_t sb = sm.stages + stage * C::kStageBytes;
 #pragma unroll
-    for (int nt = 0; nt < D / 8; ++nt) {
-        const uint32_t v = pack_bf16x2(o[nt][2 * half] * inv_l, o[nt][2 * half + 1] * inv_l);
-        *reinterpret_cast<uint32_t *>(dst + nt * 8 + 2 * c) = v;
+            for (int c = 0; c < C::kChunks; ++c) {
+                tma_load_4d(sb + c * C::kRegionBytes, mk, c * 64, c1, c2, s.b, full);
+                tma_load_4d(sb + (C::kChunks + c) * C::kRegionBytes, mv, c * 64, c1, c2, s.b, full);
+            }
+            issued |= 1u << stage;
+            last_par = (last_par & ~(1u << stage)) | (phase << stage);
+            if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+        }
     }
-    if (a.lse && c == 0)
-        a.lse[(static_cast<int64_t>(pi.b) * a.Hq + h) * a.S + s] = (m + __log2f(l)) * kLn2;
+    // no copy may still be landing when the CTA exits
+    for (int st = 0; st < C::kStages; ++st)
+        if (issued >> st & 1u) mbar_drain(sm.full(st), last_par >> st & 1u);
 }
 
 template <int D>
-__device__ void merge_pair(const AttnArgs &a, const PairInfo &pi, int p, int c_first, int c_last) {
+__device__ void role_mma(const AttnArgs &a, Sched sch, const Smem<D> &sm, uint32_t tmem) {
+    using C = Cfg<D>;
+    const int lane = threadIdx.x & 31;
+    auto wait = [&](uint32_t bar, uint32_t par) -> bool {
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait(bar, par, sm.err, 2);
+        return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+    };
+    int stage = 0;
+    uint32_t phase = 0, qpar[2] = {0, 0}, ppar[2] = {0, 0}, pv_cnt[2] = {0, 0};
+    bool ok = true;
+    Seg s;
+    while (ok && sch.next(a, s)) {
+        for (int it = 0; it < s.ntiles && ok; ++it) {
+            const int nvalid = tile_valid(a, s, s.tile0 + it);
+            if (!wait(sm.full(stage), phase)) { ok = false; break; }
+            const uint32_t sb = sm.stages + stage * C::kStageBytes;
+            const uint32_t vb = sb + C::kChunks * C::kRegionBytes;
+            for (int h = 0; h < s.nh && ok; ++h) {
+                if (it == 0) {
+                    if (!wait(sm.q_ready(h), qpar[h])) { ok = false; break; }
+                    qpar[h] ^= 1;
+                }
+                // S_h and P_h share columns: the previous P_h V must be done reading
+                if (pv_cnt[h] > 0 && !wait(sm.pv_done(h), (pv_cnt[h] - 1) & 1)) { ok = false; break; }
+                tc_fence_after();
+                if (lane == 0) {
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t addr = sb + (kk >> 2) * C::kRegionBytes + (kk & 3) * 32;
+                        tc_mma_ts(tmem + C::colS(h), tmem + C::colQ(h) + kk * 8,
+                                  sdesc_sw128(addr, 16, 1024), C::kIdescQK, kk > 0);
+                    }
+                    tc_commit(sm.s_full(h));
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (nvalid < kTN) {
+                // V rows past the valid keys may hold anything (rows >= L_b of the
+                // cache); P is 0 there, and 0 * NaN must not reach O: zero them.
+#pragma unroll
+                for (int c = 0; c < C::kChunks; ++c) {
+                    const uint32_t base = vb + c * C::kRegionBytes;
+                    for (uint32_t off = nvalid * 128 + lane * 16; off < C::kRegionBytes; off += 512)
+                        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(base + off),
+                                     "r"(0u)
+                                     : "memory");
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+            }
+            for (int h = 0; h < s.nh && ok; ++h) {
+                if (!wait(sm.p_full(h), ppar[h])) { ok = false; break; }
+                ppar[h] ^= 1;
+                tc_fence_after();
+                if (lane == 0) {
+#pragma unroll
+                    for (int kk = 0; kk < kTN / 16; ++kk)
+                        tc_mma_ts(tmem + C::colO(h), tmem + C::colS(h) + kk * 8,
+                                  sdesc_sw128(vb + kk * 2048, C::kRegionBytes, 1024), C::kIdescPV,
+                                  (it > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit(sm.pv_done(h));
+                }
+                __syncwarp();
+                ++pv_cnt[h];
+            }
+            if (!ok) break;
+            if (lane == 0) tc_commit(sm.empty(stage));
+            __syncwarp();
+            if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+        }
+    }
+    // every MMA issued here completes before TMEM is freed
+    if (lane == 0) {
+        tc_commit(sm.fin());
+        mbar_drain(sm.fin(), 0);
+    }
+    __syncwarp();
+}
+
+template <int D>
+__device__ __forceinline__ void store_row(const AttnArgs &a, const Seg &s, int rl,
+                                          const float *o, int col0) {
+    const int rr = s.rg * kRows + rl;
+    const int sq = rr / a.G, head = s.g * a.G + rr % a.G;
+    uint16_t *dst = a.out + s.b * a.os[0] + sq * a.os[1] + head * a.os[2] + col0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint4 v;
+        v.x = pack_bf16x2(o[8 * j + 0], o[8 * j + 1]);
+        v.y = pack_bf16x2(o[8 * j + 2], o[8 * j + 3]);
+        v.z = pack_bf16x2(o[8 * j + 4], o[8 * j + 5]);
+        v.w = pack_bf16x2(o[8 * j + 6], o[8 * j + 7]);
+        *reinterpret_cast<uint4 *>(dst + 8 * j) = v;
+    }
+}
+
+__device__ __forceinline__ void store_lse(const AttnArgs &a, const Seg &s, int rl, float m_log2,
+                                          float l) {
+    if (!a.lse) return;
+    const int rr = s.rg * kRows + rl;
+    const int sq = rr / a.G, head = s.g * a.G + rr % a.G;
+    a.lse[(static_cast<int64_t>(s.b) * a.Hq + head) * a.S + sq] = (m_log2 + __log2f(l)) * kLn2;
+}
+
+template <int D>
+__device__ void role_softmax(const AttnArgs &a, Sched sch, const Smem<D> &sm, uint32_t tmem) {
+    using C = Cfg<D>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    constexpr int kPer = D / 32;  // columns per lane
-    for (int r = warp; r < pi.rows; r += kWarps) {
-        float M = -INFINITY;
-        for (int c = c_first; c <= c_last; ++c) {
-            const float2 ml = __ldcg(a.part_ml + static_cast<size_t>(c + p) * kRows + r);
-            M = fmaxf(M, ml.x);
-        }
-        float den = 0.f, acc[kPer];
+    const int h = warp >> 2, q4 = warp & 3, r = q4 * 32 + lane;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(q4 * 32) << 16);  // this warp's lanes
+    const float c = a.scale_log2;
+    auto wait = [&](uint32_t bar, uint32_t par) -> bool {
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait(bar, par, sm.err, 3);
+        return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+    };
+    uint32_t spar = 0, pv_seen = 0, wgpar = 0;
+    auto wg_sync = [&]() -> bool {
+        mbar_arrive(sm.wg_bar(h));
+        const bool ok = wait(sm.wg_bar(h), wgpar);
+        wgpar ^= 1;
+        return ok;
+    };
+    bool ok = true;
+    Seg s;
+    while (ok && sch.next(a, s)) {
+        if (h >= s.nh) continue;
+        const int rl = h * 128 + r;  // row within the pair
+        const bool valid = rl < s.rows;
+        {  // Q row -> TMEM (zeros for rows past the pair)
+            uint32_t qw[C::kQCols];
+            if (valid) {
+                const int rr = s.rg * kRows + rl;
+                const int sq = rr / a.G, head = s.g * a.G + rr % a.G;
+                const uint4 *src = reinterpret_cast<const uint4 *>(a.q + s.b * a.qs[0] +
+                                                                   sq * a.qs[1] + head * a.qs[2]);
 #pragma unroll
-        for (int j = 0; j < kPer; ++j) acc[j] = 0.f;
-        for (int c = c_first; c <= c_last; ++c) {
-            const size_t slot = static_cast<size_t>(c + p);
-            const float2 ml = __ldcg(a.part_ml + slot * kRows + r);
-            const float w = ex2_approx(ml.x - M);
-            den += w * ml.y;
-            const float *src = a.part_o + (slot * kRows + r) * D + lane * kPer;
-            if constexpr (kPer == 4) {
-                const float4 v = __ldcg(reinterpret_cast<const float4 *>(src));
-                acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
+                for (int j = 0; j < D / 8; ++j) {
+                    const uint4 v = __ldg(src + j);
+                    qw[4 * j] = v.x; qw[4 * j + 1] = v.y; qw[4 * j + 2] = v.z; qw[4 * j + 3] = v.w;
+                }
             } else {
-                const float2 v = __ldcg(reinterpret_cast<const float2 *>(src));
-                acc[0] += w * v.x; acc[1] += w * v.y;
+#pragma unroll
+                for (int j = 0; j < C::kQCols; ++j) qw[j] = 0u;
+            }
+#pragma unroll
+            for (int j = 0; j < C::kQCols / 32; ++j) tmem_st32(tl + C::colQ(h) + 32 * j, qw + 32 * j);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(sm.q_ready(h));
+        }
+        float m_run = -INFINITY, l_run = 0.f;
+        for (int it = 0; it < s.ntiles; ++it) {
+            const int nvalid = tile_valid(a, s, s.tile0 + it);
+            if (!wait(sm.s_full(h), spar)) { ok = false; break; }
+            spar ^= 1;
+            tc_fence_after();
+            uint32_t v[kTN];
+            tmem_ld32(tl + C::colS(h), v);
+            tmem_ld32(tl + C::colS(h) + 32, v + 32);
+            tmem_wait_ld(v);
+            tmem_touch(v + 32);
+            float mx = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < kTN; ++j) {
+                float x = __uint_as_float(v[j]);
+                if (nvalid < kTN && j >= nvalid) x = -INFINITY;
+                v[j] = __float_as_uint(x);
+                mx = fmaxf(mx, x);
+            }
+            const float m_tile = mx * c;
+            if (it == 0) {
+                m_run = m_tile;
+            } else {
+                const bool need = m_tile > m_run + kRescaleLog2;
+                if (__any_sync(0xFFFFFFFFu, need)) {
+                    const float f = need ? ex2_approx(m_run - m_tile) : 1.f;
+                    if (need) { l_run *= f; m_run = m_tile; }
+#pragma unroll 1
+                    for (int j = 0; j < D / 32; ++j) {
+                        uint32_t o[32];
+                        tmem_ld32(tl + C::colO(h) + 32 * j, o);
+                        tmem_wait_ld(o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+                        tmem_st32(tl + C::colO(h) + 32 * j, o);
+                    }
+                    tmem_wait_st();
+                }
+            }
+            const float neg_m = -m_run;
+            float sum = 0.f;
+            uint32_t pk[kTN / 2];
+#pragma unroll
+            for (int j = 0; j < kTN / 2; ++j) {
+                const float p0 = ex2_approx(fmaf(__uint_as_float(v[2 * j]), c, neg_m));
+                const float p1 = ex2_approx(fmaf(__uint_as_float(v[2 * j + 1]), c, neg_m));
+                sum += p0 + p1;
+                pk[j] = pack_bf16x2(p0, p1);
+            }
+            l_run += sum;
+            tmem_st32(tl + C::colS(h), pk);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(sm.p_full(h));
+            ++pv_seen;
+        }
+        if (!ok) break;
+        // ---- segment epilogue: O_h is final once the last P_h V is done
+        if (!wait(sm.pv_done(h), (pv_seen - 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        if (s.c_first == s.c_last) {
+            const float inv = 1.f / l_run;
+#pragma unroll 1
+            for (int j = 0; j < D / 32; ++j) {
+                uint32_t o[32];
+                tmem_ld32(tl + C::colO(h) + 32 * j, o);
+                tmem_wait_ld(o);
+                if (valid) {
+                    float f[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(o[e]) * inv;
+                    store_row<D>(a, s, rl, f, 32 * j);
+                }
+            }
+            if (valid) store_lse(a, s, rl, m_run, l_run);
+            continue;
+        }
+        // ---- split pair: write this CTA's partial, the last CTA to arrive merges
+        const int cta = blockIdx.x;
+        const size_t slot = static_cast<size_t>(cta + s.p);
+#pragma unroll 1
+        for (int j = 0; j < D / 32; ++j) {
+            uint32_t o[32];
+            tmem_ld32(tl + C::colO(h) + 32 * j, o);
+            tmem_wait_ld(o);
+            if (valid) {
+                float *dst = a.part_o + (slot * D + 32 * j) * kRows + rl;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) __stcg(dst + e * kRows, __uint_as_float(o[e]));
             }
         }
-        const float inv = 1.f / den;
-        const int rr = pi.rg * kRows + r;
-        const int s = rr / a.G, h = pi.g * a.G + rr % a.G;
-        uint16_t *dst = a.out + pi.b * a.os[0] + s * a.os[1] + h * a.os[2] + lane * kPer;
-        if constexpr (kPer == 4) {
-            uint2 v;
-            v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-            v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-            *reinterpret_cast<uint2 *>(dst) = v;
-        } else {
-            *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        if (valid) __stcg(a.part_ml + slot * kRows + rl, make_float2(m_run, l_run));
+        __threadfence();
+        if (!wg_sync()) { ok = false; break; }
+        if (r == 0) {
+            const unsigned old = atomicAdd(a.pair_cnt + 2 * s.p + h, 1u);
+            sm.last[h] = old == static_cast<unsigned>(s.c_last - s.c_first);
         }
-        if (a.lse && lane == 0)
-            a.lse[(static_cast<int64_t>(pi.b) * a.Hq + h) * a.S + s] = (M + __log2f(den)) * kLn2;
+        if (!wg_sync()) { ok = false; break; }
+        if (!sm.last[h]) continue;
+        __threadfence();
+        if (valid) {
+            float M = -INFINITY;
+            for (int cc = s.c_first; cc <= s.c_last; ++cc)
+                M = fmaxf(M, __ldcg(a.part_ml + static_cast<size_t>(cc + s.p) * kRows + rl).x);
+            float den = 0.f;
+            for (int cc = s.c_first; cc <= s.c_last; ++cc) {
+                const float2 ml = __ldcg(a.part_ml + static_cast<size_t>(cc + s.p) * kRows + rl);
+                den += ex2_approx(ml.x - M) * ml.y;
+            }
+            const float inv = 1.f / den;
+#pragma unroll 1
+            for (int j = 0; j < D / 32; ++j) {
+                float acc[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+                for (int cc = s.c_first; cc <= s.c_last; ++cc) {
+                    const size_t sl = static_cast<size_t>(cc + s.p);
+                    const float w = ex2_approx(__ldcg(a.part_ml + sl * kRows + rl).x - M) * inv;
+                    const float *src = a.part_o + (sl * D + 32 * j) * kRows + rl;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) acc[e] += w * __ldcg(src + e * kRows);
+                }
+                store_row<D>(a, s, rl, acc, 32 * j);
+            }
+            store_lse(a, s, rl, M, den);
+        }
+        if (r == 0) a.pair_cnt[2 * s.p + h] = 0u;
     }
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) block_attn_mma_kernel(const AttnArgs a) {
-    extern __shared__ __align__(128) unsigned char smem[];
-    uint16_t *qs = reinterpret_cast<uint16_t *>(smem);
-    uint16_t *stage0 = reinterpret_cast<uint16_t *>(smem + Layout<D>::kQBytes);
-    int *prefix = reinterpret_cast<int *>(smem + Layout<D>::kBytes);  // [npairs + 1]
-    __shared__ int warp_sums[kWarps];
-    __shared__ int is_last;
+__global__ void __launch_bounds__(kThreads, 1)
+    block_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
+                         const __grid_constant__ CUtensorMap tm_vc,
+                         const __grid_constant__ CUtensorMap tm_kb,
+                         const __grid_constant__ CUtensorMap tm_vb, const AttnArgs a) {
+    using C = Cfg<D>;
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    unsigned char *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // 1024-byte aligned
+    int *prefix = reinterpret_cast<int *>(smem + C::kPrefixOffset);
+    int *misc = reinterpret_cast<int *>(smem + C::kMiscOffset);
+    __shared__ int warp_sums[kThreads / 32];
 
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    constexpr int kWarps = kThreads / 32;
 
     // ---- tile counts per pair and their exclusive prefix sum
     {
@@ -255,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1) block_attn_mma_kernel(const AttnA
                 const int v = __shfl_up_sync(0xFFFFFFFFu, w, off);
                 if (lane >= off) w += v;
             }
-            if (lane < kWarps) warp_sums[lane] = w;  // inclusive warp totals
+            if (lane < kWarps) warp_sums[lane] = w;
         }
         __syncthreads();
         int run = incl - local + (warp > 0 ? warp_sums[warp - 1] : 0);
@@ -274,181 +680,66 @@ __global__ void __launch_bounds__(kThreads, 1) block_attn_mma_kernel(const AttnA
     const int P = static_cast<int>(parts);
     const int cta = blockIdx.x;
     if (cta >= P) return;
-    const int64_t t_begin = static_cast<int64_t>(cta) * T / P;
-    const int64_t t_end = static_cast<int64_t>(cta + 1) * T / P;
 
-    const int g8 = lane >> 2, c4 = lane & 3;
-    const int row0 = warp * 16;
-
-    for (int64_t tcur = t_begin; tcur < t_end;) {
-        // pair holding tile tcur: last p with prefix[p] <= tcur
-        int lo = 0, hi = a.npairs;  // invariant: prefix[lo] <= tcur < prefix[hi]
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (prefix[mid] <= tcur) lo = mid; else hi = mid;
+    Smem<D> sm;
+    sm.stages = smem_u32(smem);
+    sm.bars = smem_u32(smem + C::kBarOffset);
+    sm.prefix = prefix;
+    sm.tmem_slot = reinterpret_cast<uint32_t *>(misc);
+    sm.err = misc + 1;
+    sm.last = misc + 2;
+    if (t == 0) {
+        for (int i = 0; i < C::kStages; ++i) {
+            mbar_init(sm.full(i), 1);
+            mbar_init(sm.empty(i), 1);
         }
-        const int p = lo;
-        const int64_t ps = prefix[p], pe = prefix[p + 1];
-        const int64_t seg_end = min(t_end, pe);
-        const PairInfo pi = pair_info(a, p);
-        const int tile0 = static_cast<int>(tcur - ps), ntiles = static_cast<int>(seg_end - tcur);
-        const int c_first = owner_of(ps, P, T), c_last = owner_of(pe - 1, P, T);
-
-        // ---- pipeline prologue: Q, then the first kStages-1 tiles
-        load_q<D>(a, pi, qs);
-        cp_async_commit();
-#pragma unroll
-        for (int st = 0; st < kStages - 1; ++st) {
-            if (st < ntiles) {
-                uint16_t *ks = stage0 + st * (Layout<D>::kStageBytes / 2);
-                load_tile<D>(a, pi, tile0 + st, ks, ks + Layout<D>::kTileBytes / 2);
-            }
-            cp_async_commit();
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(sm.s_full(h), 1);
+            mbar_init(sm.p_full(h), 128);
+            mbar_init(sm.pv_done(h), 1);
+            mbar_init(sm.q_ready(h), 128);
+            mbar_init(sm.wg_bar(h), 128);
         }
-
-        float o[D / 8][4];
-#pragma unroll
-        for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-        float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-
-        for (int it = 0; it < ntiles; ++it) {
-            cp_async_wait<kStages - 2>();
-            __syncthreads();
-            {  // refill the stage freed by the previous tile
-                const int nt_load = it + kStages - 1;
-                if (nt_load < ntiles) {
-                    uint16_t *ks = stage0 + (nt_load % kStages) * (Layout<D>::kStageBytes / 2);
-                    load_tile<D>(a, pi, tile0 + nt_load, ks, ks + Layout<D>::kTileBytes / 2);
-                }
-                cp_async_commit();
-            }
-            const uint16_t *ks = stage0 + (it % kStages) * (Layout<D>::kStageBytes / 2);
-            const uint16_t *vs = ks + Layout<D>::kTileBytes / 2;
-            const int tile = tile0 + it;
-            const bool block_tile = tile == pi.nctx_tiles;
-            const int nvalid = block_tile ? a.S : min(kTN, pi.L - tile * kTN);
-
-            // S = Q K^T for this warp's 16 rows x 64 keys
-            float sc[kTN / 8][4];
-#pragma unroll
-            for (int i = 0; i < kTN / 8; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                uint32_t af[4];
-                {
-                    const int mi = lane >> 3;
-                    const int r = row0 + (mi & 1) * 8 + (lane & 7);
-                    const int col = kk * 16 + (mi >> 1) * 8;
-                    ldsm_x4(smem_u32(qs + r * Layout<D>::kStride + col), af);
-                }
-#pragma unroll
-                for (int np = 0; np < kTN / 16; ++np) {
-                    uint32_t bf[4];
-                    const int mi = lane >> 3;
-                    const int key = np * 16 + (mi >> 1) * 8 + (lane & 7);
-                    const int col = kk * 16 + (mi & 1) * 8;
-                    ldsm_x4(smem_u32(ks + key * Layout<D>::kStride + col), bf);
-                    mma_bf16(sc[2 * np], af, bf[0], bf[1]);
-                    mma_bf16(sc[2 * np + 1], af, bf[2], bf[3]);
-                }
-            }
-            // online softmax (exp2 domain), two rows per thread: g8 and g8+8
-#pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-                float mx = -INFINITY;
-#pragma unroll
-                for (int nt = 0; nt < kTN / 8; ++nt) {
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int key = nt * 8 + 2 * c4 + e;
-                        float x = sc[nt][2 * hr + e] * a.scale_log2;
-                        x = key < nvalid ? x : -INFINITY;
-                        sc[nt][2 * hr + e] = x;
-                        mx = fmaxf(mx, x);
-                    }
-                }
-                mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-                mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
-                const float mnew = fmaxf(m[hr], mx);
-                const float corr = ex2_approx(m[hr] - mnew);
-                m[hr] = mnew;
-                l[hr] *= corr;
-#pragma unroll
-                for (int i = 0; i < D / 8; ++i) {
-                    o[i][2 * hr] *= corr;
-                    o[i][2 * hr + 1] *= corr;
-                }
-                float ls = 0.f;
-#pragma unroll
-                for (int nt = 0; nt < kTN / 8; ++nt) {
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const float pv = ex2_approx(sc[nt][2 * hr + e] - mnew);
-                        sc[nt][2 * hr + e] = pv;
-                        ls += pv;
-                    }
-                }
-                l[hr] += ls;
-            }
-            // O += P V
-#pragma unroll
-            for (int j = 0; j < kTN / 16; ++j) {
-                uint32_t pf[4];
-                pf[0] = pack_bf16x2(sc[2 * j][0], sc[2 * j][1]);
-                pf[1] = pack_bf16x2(sc[2 * j][2], sc[2 * j][3]);
-                pf[2] = pack_bf16x2(sc[2 * j + 1][0], sc[2 * j + 1][1]);
-                pf[3] = pack_bf16x2(sc[2 * j + 1][2], sc[2 * j + 1][3]);
-#pragma unroll
-                for (int dp = 0; dp < D / 16; ++dp) {
-                    uint32_t bf[4];
-                    const int mi = lane >> 3;
-                    const int key = j * 16 + (mi & 1) * 8 + (lane & 7);
-                    const int col = dp * 16 + (mi >> 1) * 8;
-                    ldsm_x4_t(smem_u32(vs + key * Layout<D>::kStride + col), bf);
-                    mma_bf16(o[2 * dp], pf, bf[0], bf[1]);
-                    mma_bf16(o[2 * dp + 1], pf, bf[2], bf[3]);
-                }
-            }
-        }
-        cp_async_wait<0>();
-        __syncthreads();  // stages and Q are free for the next segment
-
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-            l[hr] += __shfl_xor_sync(0xFFFFFFFFu, l[hr], 1);
-            l[hr] += __shfl_xor_sync(0xFFFFFFFFu, l[hr], 2);
-        }
-        if (c_first == c_last) {
-#pragma unroll
-            for (int hr = 0; hr < 2; ++hr)
-                store_rows<D>(a, pi, row0 + g8 + 8 * hr, o, hr, 1.f / l[hr], m[hr], l[hr]);
-        } else {
-            const size_t slot = static_cast<size_t>(cta + p);
-#pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-                const int r = row0 + g8 + 8 * hr;
-                float *dst = a.part_o + (slot * kRows + r) * D;
-#pragma unroll
-                for (int nt = 0; nt < D / 8; ++nt)
-                    *reinterpret_cast<float2 *>(dst + nt * 8 + 2 * c4) =
-                        make_float2(o[nt][2 * hr], o[nt][2 * hr + 1]);
-                if (c4 == 0) a.part_ml[slot * kRows + r] = make_float2(m[hr], l[hr]);
-            }
-            __syncthreads();
-            if (t == 0) {
-                __threadfence();
-                const unsigned old = atomicAdd(a.pair_cnt + p, 1u);
-                is_last = old == static_cast<unsigned>(c_last - c_first);
-                if (is_last) __threadfence();
-            }
-            __syncthreads();
-            if (is_last) {
-                merge_pair<D>(a, pi, p, c_first, c_last);
-                if (t == 0) a.pair_cnt[p] = 0;
-            }
-        }
-        tcur = seg_end;
+        mbar_init(sm.fin(), 1);
+        *sm.err = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if (warp == kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(sm.tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *sm.tmem_slot;
+
+    Sched sch;
+    sch.prefix = prefix;
+    sch.P = P;
+    sch.T = T;
+    sch.tcur = static_cast<int64_t>(cta) * T / P;
+    sch.tend = static_cast<int64_t>(cta + 1) * T / P;
+
+    if (warp == kProducerWarp) {
+        if (lane == 0) role_producer<D>(a, sch, sm, &tm_kc, &tm_vc, &tm_kb, &tm_vb);
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        role_mma<D>(a, sch, sm, tmem);
+    } else {
+        role_softmax<D>(a, sch, sm, tmem);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kMmaWarp)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols)
+                     : "memory");
+    if (t == 0 && *sm.err) atomicOr(a.err_word, *sm.err);
 }
 
 // ---------------------------------------------------------------- host
@@ -481,6 +772,8 @@ tt_status validate(const tt_attn_desc *d, Geometry *geo, const char *fn) {
     if (np > kMaxPairs)
         return fail(TT_ERR_UNSUPPORTED, "%s: B*Hkv*ceil(S*Hq/Hkv/256) = %lld > %d", fn,
                     (long long)np, kMaxPairs);
+    if (np * ((static_cast<int64_t>(d->Lmax) + kTN - 1) / kTN + 1) >= (int64_t(1) << 31))
+        return fail(TT_ERR_UNSUPPORTED, "%s: more than 2^31 key tiles", fn);
     geo->npairs = static_cast<int>(np);
     geo->P = sm_count();
     if (geo->P <= 0) return fail(TT_ERR_CUDA, "%s: no CUDA device", fn);
@@ -488,60 +781,111 @@ tt_status validate(const tt_attn_desc *d, Geometry *geo, const char *fn) {
 }
 
 struct AttnWs {
+    int *err_word;
     unsigned *pair_cnt;
     float2 *part_ml;
     float *part_o;
     size_t bytes;
 };
 
-AttnWs carve_attn(void *ws, const tt_attn_desc *d, const Geometry &g) {
-    Carve c(ws);
+AttnWs carve(void *base, int npairs, size_t slots, int d) {
+    Carve c(base);
     AttnWs w;
-    const size_t slots = static_cast<size_t>(g.P) + g.npairs;
-    w.pair_cnt = c.take<unsigned>(static_cast<size_t>(g.npairs));
+    w.err_word = c.take<int>(1);
+    w.pair_cnt = c.take<unsigned>(2 * static_cast<size_t>(npairs));
     w.part_ml = c.take<float2>(slots * kRows);
-    w.part_o = c.take<float>(slots * kRows * d->d);
+    w.part_o = c.take<float>(slots * kRows * d);
     w.bytes = c.bytes();
     return w;
 }
 
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// 4-D bf16 tensor map, 128-byte swizzle, box (64, b1, b2, 1); strides in elements.
+tt_status make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+                   uint64_t d3, int64_t s1, int64_t s2, int64_t s3, uint32_t b1, uint32_t b2,
+                   const char *fn, const char *what) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return fail(TT_ERR_CUDA, "%s: cuTensorMapEncodeTiled unavailable", fn);
+    const cuuint64_t dims[4] = {d0, d1, d2, d3};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(s1) * 2, static_cast<cuuint64_t>(s2) * 2,
+                                   static_cast<cuuint64_t>(s3) * 2};
+    const cuuint32_t box[4] = {64, b1, b2, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
+                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(TT_ERR_UNSUPPORTED, "%s: tensor map for %s rejected (CUresult %d)", fn, what,
+                    static_cast<int>(r));
+    return TT_OK;
+}
+
 template <int D>
-tt_status launch(const AttnArgs &a, int smem_bytes, cudaStream_t stream) {
+tt_status launch(const tt_attn_desc *d, const AttnArgs &a, const void *k_ctx, const void *v_ctx,
+                 const void *k_blk, const void *v_blk, cudaStream_t stream, const char *fn) {
+    CUtensorMap kc, vc, kb, vb;
+    tt_status st;
+    const uint64_t B = d->B, S = d->S, Hkv = d->Hkv, Lmax = d->Lmax;
+    if ((st = make_map(&kb, k_blk, D, Hkv, S, B, d->kblk_strides[2], d->kblk_strides[1],
+                       d->kblk_strides[0], 1, 64, fn, "k_blk")) != TT_OK)
+        return st;
+    if ((st = make_map(&vb, v_blk, D, Hkv, S, B, d->vblk_strides[2], d->vblk_strides[1],
+                       d->vblk_strides[0], 1, 64, fn, "v_blk")) != TT_OK)
+        return st;
+    if (Lmax > 0) {
+        if ((st = make_map(&kc, k_ctx, D, Lmax, Hkv, B, d->kctx_strides[2], d->kctx_strides[1],
+                           d->kctx_strides[0], 64, 1, fn, "k_ctx")) != TT_OK)
+            return st;
+        if ((st = make_map(&vc, v_ctx, D, Lmax, Hkv, B, d->vctx_strides[2], d->vctx_strides[1],
+                           d->vctx_strides[0], 64, 1, fn, "v_ctx")) != TT_OK)
+            return st;
+    } else {  // no context rows: the context maps are never used
+        kc = kb;
+        vc = vb;
+    }
+    static std::mutex mu;
     static bool configured[64] = {false};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(block_attn_mma_kernel<D>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             smem_bytes > 200 * 1024 ? smem_bytes : 200 * 1024);
-        if (e != cudaSuccess) return cuda_status(e, "tt_block_attn: smem attribute");
-        configured[dev] = true;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev < 64 && !configured[dev]) {
+            cudaError_t e = cudaFuncSetAttribute(block_attn_tc_kernel<D>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 Cfg<D>::smem_bytes(kMaxPairs));
+            if (e != cudaSuccess) return cuda_status(e, "tt_block_attn: smem attribute");
+            configured[dev] = true;
+        }
     }
-    block_attn_mma_kernel<D><<<a.P, kThreads, smem_bytes, stream>>>(a);
+    block_attn_tc_kernel<D><<<a.P, kThreads, Cfg<D>::smem_bytes(a.npairs), stream>>>(kc, vc, kb,
+                                                                                    vb, a);
     return cuda_status(cudaGetLastError(), "tt_block_attn launch");
 }
 
-}  // namespace
-}  // namespace tt
-
-using namespace tt;
-
-extern "C" {
-
-size_t tt_block_attn_workspace_size(const tt_attn_desc *d) {
-    Geometry g;
-    if (validate(d, &g, "tt_block_attn_workspace_size") != TT_OK) return 0;
-    return carve_attn(nullptr, d, g).bytes;
-}
-
-tt_status tt_block_attn(const tt_attn_desc *d, const void *q, const void *k_ctx, const void *v_ctx,
-                        const int32_t *ctx_lens, const void *k_blk, const void *v_blk, void *out,
-                        float *lse, void *workspace, size_t workspace_bytes, tt_stream_t stream) {
-    const char *fn = "tt_block_attn";
-    Geometry g;
-    tt_status st = validate(d, &g, fn);
-    if (st != TT_OK) return st;
-    if (d->B == 0) return TT_OK;
+tt_status check_ptrs(const tt_attn_desc *d, const void *q, const void *k_ctx, const void *v_ctx,
+                     const int32_t *ctx_lens, const void *k_blk, const void *v_blk,
+                     const void *out, const float *lse, const char *fn) {
     if (!q || !k_blk || !v_blk || !out || !ctx_lens || (d->Lmax > 0 && (!k_ctx || !v_ctx)))
         return fail(TT_ERR_INVALID_ARG, "%s: null pointer", fn);
     const void *ptrs[6] = {q, k_ctx, v_ctx, k_blk, v_blk, out};
@@ -550,27 +894,18 @@ tt_status tt_block_attn(const tt_attn_desc *d, const void *q, const void *k_ctx,
             return fail(TT_ERR_INVALID_ARG, "%s: tensor base not 16-byte aligned", fn);
     if (reinterpret_cast<uintptr_t>(ctx_lens) % 4 || (lse && reinterpret_cast<uintptr_t>(lse) % 4))
         return fail(TT_ERR_INVALID_ARG, "%s: ctx_lens/lse misaligned", fn);
-    AttnWs w = carve_attn(workspace, d, g);
-    if (!workspace || workspace_bytes < w.bytes)
-        return fail(TT_ERR_WORKSPACE, "%s: workspace of %zu bytes, %zu needed", fn, workspace_bytes,
-                    w.bytes);
-    if (reinterpret_cast<uintptr_t>(workspace) % 256)
-        return fail(TT_ERR_WORKSPACE, "%s: workspace not 256-byte aligned", fn);
+    return TT_OK;
+}
 
+tt_status run(const tt_attn_desc *d, const Geometry &g, const AttnWs &w, const void *q,
+              const void *k_ctx, const void *v_ctx, const int32_t *ctx_lens, const void *k_blk,
+              const void *v_blk, void *out, float *lse, cudaStream_t stream, const char *fn) {
     AttnArgs a;
     a.q = static_cast<const uint16_t *>(q);
-    a.kctx = static_cast<const uint16_t *>(k_ctx ? k_ctx : q);
-    a.vctx = static_cast<const uint16_t *>(v_ctx ? v_ctx : q);
-    a.kblk = static_cast<const uint16_t *>(k_blk);
-    a.vblk = static_cast<const uint16_t *>(v_blk);
     a.out = static_cast<uint16_t *>(out);
     a.lse = lse;
     for (int i = 0; i < 4; ++i) {
         a.qs[i] = d->q_strides[i];
-        a.kcs[i] = d->kctx_strides[i];
-        a.vcs[i] = d->vctx_strides[i];
-        a.kbs[i] = d->kblk_strides[i];
-        a.vbs[i] = d->vblk_strides[i];
         a.os[i] = d->o_strides[i];
     }
     a.lens = ctx_lens;
@@ -589,9 +924,49 @@ tt_status tt_block_attn(const tt_attn_desc *d, const void *q, const void *k_ctx,
     a.part_o = w.part_o;
     a.part_ml = w.part_ml;
     a.pair_cnt = w.pair_cnt;
-    const int extra = (g.npairs + 1) * static_cast<int>(sizeof(int));
-    if (d->d == 128) return launch<128>(a, Layout<128>::kBytes + extra, (cudaStream_t)stream);
-    return launch<64>(a, Layout<64>::kBytes + extra, (cudaStream_t)stream);
+    a.err_word = w.err_word;
+    if (d->d == 128) return launch<128>(d, a, k_ctx, v_ctx, k_blk, v_blk, stream, fn);
+    return launch<64>(d, a, k_ctx, v_ctx, k_blk, v_blk, stream, fn);
+}
+
+}  // namespace
+}  // namespace tt
+
+using namespace tt;
+
+extern "C" {
+
+size_t tt_block_attn_workspace_size(const tt_attn_desc *d) {
+    Geometry g;
+    if (validate(d, &g, "tt_block_attn_workspace_size") != TT_OK) return 0;
+    return carve(nullptr, g.npairs, static_cast<size_t>(g.P) + g.npairs, d->d).bytes;
+}
+
+tt_status tt_block_attn(const tt_attn_desc *d, const void *q, const void *k_ctx, const void *v_ctx,
+                        const int32_t *ctx_lens, const void *k_blk, const void *v_blk, void *out,
+                        float *lse, void *workspace, size_t workspace_bytes, tt_stream_t stream) {
+    const char *fn = "tt_block_attn";
+    Geometry g;
+    tt_status st = validate(d, &g, fn);
+    if (st != TT_OK) return st;
+    if (d->B == 0) return TT_OK;
+    if ((st = check_ptrs(d, q, k_ctx, v_ctx, ctx_lens, k_blk, v_blk, out, lse, fn)) != TT_OK)
+        return st;
+    AttnWs w = carve(workspace, g.npairs, static_cast<size_t>(g.P) + g.npairs, d->d);
+    if (!workspace || workspace_bytes < w.bytes)
+        return fail(TT_ERR_WORKSPACE, "%s: workspace of %zu bytes, %zu needed", fn, workspace_bytes,
+                    w.bytes);
+    if (reinterpret_cast<uintptr_t>(workspace) % 256)
+        return fail(TT_ERR_WORKSPACE, "%s: workspace not 256-byte aligned", fn);
+    return run(d, g, w, q, k_ctx, v_ctx, ctx_lens, k_blk, v_blk, out, lse, (cudaStream_t)stream, fn);
+}
+
+tt_status tt_block_attn_error(const void *workspace, int32_t *flag_out, tt_stream_t stream) {
+    if (!workspace || !flag_out) return fail(TT_ERR_INVALID_ARG, "tt_block_attn_error: null pointer");
+    cudaError_t e = cudaMemcpyAsync(flag_out, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost,
+                                    (cudaStream_t)stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+    return cuda_status(e, "tt_block_attn_error");
 }
 
 }  // extern "C"
@@ -627,17 +1002,6 @@ tt_status static_scratch(void **out, const char *fn) {
     return TT_OK;
 }
 
-// Layout of the static scratch for `slots` partial slots.
-AttnWs carve_static(void *base, int npairs, size_t slots, int d) {
-    Carve c(base);
-    AttnWs w;
-    w.pair_cnt = c.take<unsigned>(static_cast<size_t>(npairs));
-    w.part_ml = c.take<float2>(slots * kRows);
-    w.part_o = c.take<float>(slots * kRows * d);
-    w.bytes = c.bytes();
-    return w;
-}
-
 }  // namespace
 }  // namespace tt
 
@@ -652,19 +1016,11 @@ extern "C" tt_status tt_block_attn_noalloc(const tt_attn_desc *d, const void *q,
     tt_status st = validate(d, &g, fn);
     if (st != TT_OK) return st;
     if (d->B == 0) return TT_OK;
-    if (!q || !k_blk || !v_blk || !out || !ctx_lens || (d->Lmax > 0 && (!k_ctx || !v_ctx)))
-        return fail(TT_ERR_INVALID_ARG, "%s: null pointer", fn);
-    const void *ptrs[6] = {q, k_ctx, v_ctx, k_blk, v_blk, out};
-    for (int i = 0; i < 6; ++i)
-        if (reinterpret_cast<uintptr_t>(ptrs[i]) % 16)
-            return fail(TT_ERR_INVALID_ARG, "%s: tensor base not 16-byte aligned", fn);
-    if (reinterpret_cast<uintptr_t>(ctx_lens) % 4 || (lse && reinterpret_cast<uintptr_t>(lse) % 4))
-        return fail(TT_ERR_INVALID_ARG, "%s: ctx_lens/lse misaligned", fn);
-    // slots that fit: one per pair plus at least one partition
-    const size_t per_slot = carve_static(nullptr, 0, 1, d->d).bytes;
-    size_t slots = kStaticScratchBytes / per_slot;
-    while (slots > 0 && carve_static(nullptr, g.npairs, slots, d->d).bytes > kStaticScratchBytes)
-        --slots;
+    if ((st = check_ptrs(d, q, k_ctx, v_ctx, ctx_lens, k_blk, v_blk, out, lse, fn)) != TT_OK)
+        return st;
+    // partial slots that fit: one per pair plus at least one partition
+    size_t slots = kStaticScratchBytes / carve(nullptr, 0, 1, d->d).bytes;
+    while (slots > 0 && carve(nullptr, g.npairs, slots, d->d).bytes > kStaticScratchBytes) --slots;
     if (slots < static_cast<size_t>(g.npairs) + 1)
         return fail(TT_ERR_UNSUPPORTED,
                     "%s: B*Hkv*ceil(S*Hq/Hkv/256) = %d pairs need more than the %zu-byte static "
@@ -674,45 +1030,10 @@ extern "C" tt_status tt_block_attn_noalloc(const tt_attn_desc *d, const void *q,
     if (static_cast<size_t>(g.P) > parts) g.P = static_cast<int>(parts);
     void *base = nullptr;
     if ((st = static_scratch(&base, fn)) != TT_OK) return st;
-    AttnWs w = carve_static(base, g.npairs, static_cast<size_t>(g.P) + g.npairs, d->d);
-    // the arrival counters must start at zero whatever an earlier call left behind
-    st = cuda_status(cudaMemsetAsync(w.pair_cnt, 0, sizeof(unsigned) * g.npairs,
-                                     (cudaStream_t)stream), fn);
+    AttnWs w = carve(base, g.npairs, static_cast<size_t>(g.P) + g.npairs, d->d);
+    // the error word and arrival counters must start at zero whatever an earlier call left
+    const size_t head = reinterpret_cast<char *>(w.part_ml) - reinterpret_cast<char *>(base);
+    st = cuda_status(cudaMemsetAsync(base, 0, head, (cudaStream_t)stream), fn);
     if (st != TT_OK) return st;
-
-    AttnArgs a;
-    a.q = static_cast<const uint16_t *>(q);
-    a.kctx = static_cast<const uint16_t *>(k_ctx ? k_ctx : q);
-    a.vctx = static_cast<const uint16_t *>(v_ctx ? v_ctx : q);
-    a.kblk = static_cast<const uint16_t *>(k_blk);
-    a.vblk = static_cast<const uint16_t *>(v_blk);
-    a.out = static_cast<uint16_t *>(out);
-    a.lse = lse;
-    for (int i = 0; i < 4; ++i) {
-        a.qs[i] = d->q_strides[i];
-        a.kcs[i] = d->kctx_strides[i];
-        a.vcs[i] = d->vctx_strides[i];
-        a.kbs[i] = d->kblk_strides[i];
-        a.vbs[i] = d->vblk_strides[i];
-        a.os[i] = d->o_strides[i];
-    }
-    a.lens = ctx_lens;
-    a.B = d->B;
-    a.S = d->S;
-    a.Hq = d->Hq;
-    a.Hkv = d->Hkv;
-    a.G = g.G;
-    a.Lmax = d->Lmax;
-    a.R = g.R;
-    a.NRG = g.NRG;
-    a.npairs = g.npairs;
-    a.P = g.P;
-    const double scale = d->scale > 0.f ? d->scale : 1.0 / sqrt(static_cast<double>(d->d));
-    a.scale_log2 = static_cast<float>(scale * 1.4426950408889634);
-    a.part_o = w.part_o;
-    a.part_ml = w.part_ml;
-    a.pair_cnt = w.pair_cnt;
-    const int extra = (g.npairs + 1) * static_cast<int>(sizeof(int));
-    if (d->d == 128) return launch<128>(a, Layout<128>::kBytes + extra, (cudaStream_t)stream);
-    return launch<64>(a, Layout<64>::kBytes + extra, (cudaStream_t)stream);
+    return run(d, g, w, q, k_ctx, v_ctx, ctx_lens, k_blk, v_blk, out, lse, (cudaStream_t)stream, fn);
 }

@@ -74,6 +74,7 @@ def load(path: str = LIB_PATH):
         "tt_block_attn_workspace_size": (_sz, [ctypes.POINTER(AttnDesc)]),
         "tt_block_attn": (ctypes.c_int, [ctypes.POINTER(AttnDesc), _p, _p, _p, _p, _p, _p, _p, _p,
                                          _p, _sz, _p]),
+        "tt_block_attn_error": (ctypes.c_int, [_p, ctypes.POINTER(_i32), _p]),
         "tt_confidence_unmask_workspace_size": (_sz, [ctypes.POINTER(UnmaskDesc)]),
         "tt_confidence_unmask": (ctypes.c_int, [ctypes.POINTER(UnmaskDesc), _p, _p, _p, _p, _p, _p,
                                                 _i32, _p, _sz, _p]),
@@ -346,7 +347,8 @@ def denoise_block_loop(B: int, S: int, V: int, logits_dtype: int, temperature: f
 def exported_symbols() -> list:
     """Names of the entry points this binding expects libtt.so to export."""
     return ["tt_status_string", "tt_last_error", "tt_abi_version", "tt_workspace_zero",
-            "tt_block_attn_workspace_size", "tt_block_attn", "tt_block_attn_noalloc",
+            "tt_block_attn_workspace_size", "tt_block_attn", "tt_block_attn_error",
+            "tt_block_attn_noalloc",
             "tt_confidence_unmask_workspace_size",
             "tt_confidence_unmask", "tt_block_init", "tt_denoise_block_loop_workspace_size",
             "tt_denoise_block_loop",

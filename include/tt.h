@@ -103,7 +103,11 @@ tt_status tt_workspace_zero(void *workspace, size_t bytes, tt_stream_t stream);
  * other strides positive multiples of 8 elements so rows start on 16 bytes):
  *   q      [B, S, Hq, d]      bf16   block queries
  *   k_ctx  [B, Hkv, Lmax, d]  bf16   context-tower layer-i keys (prefix rows
- *   v_ctx  [B, Hkv, Lmax, d]  bf16   0..L_b-1 are read; rows >= L_b never are)
+ *   v_ctx  [B, Hkv, Lmax, d]  bf16   0..L_b-1; rows >= L_b never affect the
+ *                                    result, whatever they hold: the kernel
+ *                                    fetches keys in tiles of 64 rows, so rows
+ *                                    of the last partial tile below Lmax may be
+ *                                    read, and are masked out of the softmax)
  *   k_blk  [B, S, Hkv, d]     bf16   the block's own keys and values
  *   v_blk  [B, S, Hkv, d]     bf16
  *   out    [B, S, Hq, d]      bf16   written, round-to-nearest-even of fp32
@@ -137,12 +141,23 @@ size_t tt_block_attn_workspace_size(const tt_attn_desc *desc);
  *             aligned, zeroed before first use (see conventions).
  * The kernels split long prefixes across SMs and merge the partial softmax
  * states with a log-sum-exp merge; the result does not depend on the split
- * beyond fp32 rounding.
+ * beyond fp32 rounding.  The kernel's internal waits are bounded (2 s each): a
+ * wait that runs out -- which a correct build never does -- stops the kernel
+ * cleanly, leaves `out` incomplete and records a nonzero flag in the workspace
+ * (see tt_block_attn_error).
  */
 tt_status tt_block_attn(const tt_attn_desc *desc, const void *q, const void *k_ctx,
                         const void *v_ctx, const int32_t *ctx_lens, const void *k_blk,
                         const void *v_blk, void *out, float *lse, void *workspace,
                         size_t workspace_bytes, tt_stream_t stream);
+
+/*
+ * Reads the device error flag of an attention workspace into *flag_out (host):
+ * 0 = no kernel that used the workspace has given up on a wait since it was
+ * zeroed; otherwise the role that timed out first (1 = TMA producer, 2 = MMA
+ * issuer, 3 = softmax warps).  Synchronizes `stream`.
+ */
+tt_status tt_block_attn_error(const void *workspace, int32_t *flag_out, tt_stream_t stream);
 
 /*
  * tt_block_attn without a caller-provided workspace.  The TwoTower pages have

@@ -36,7 +36,7 @@ def test_block_sizes_and_head_groups(S, Hq, Hkv):
     _gpu.check_attn(synth.attn_inputs(shape, seed=S * 100 + Hq), what=f"S={S} Hq={Hq} Hkv={Hkv}")
 
 
-def test_nan_padding_is_never_read():
+def test_nan_padding_never_affects_the_result():
     shape = synth.AttnShape(3, 16, 8, 2, 128, 512, lens=[512, 100, 0])
     inp = synth.attn_inputs(shape, seed=3, nan_pad=True)
     _gpu.check_attn(inp, what="nan padded")
