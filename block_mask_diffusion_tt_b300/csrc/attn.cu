@@ -48,10 +48,13 @@ namespace {
 constexpr int kRows = 256;  // query rows per pair (two halves of 128)
 constexpr int kTN = 64;     // keys per tile
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kMmaWarp = 9;  // warps 9 and 10: MMA issuers of half 0 and half 1
+constexpr int kThreads = 352;
 constexpr int kMaxPairs = 4096;
 constexpr int kMinTiles = 4;  // smallest tile range worth a partial
+// Cost of starting a segment (Q load, pipeline refill, epilogue), in tile units: every
+// pair is charged this many extra units at its start when the tile ranges are cut.
+constexpr int kSegCost = 3;
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kRescaleLog2 = 8.f;  // lazy rescale: O is rescaled when the max grows by > 2^8
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -62,20 +65,24 @@ struct Cfg {
     static constexpr int kChunks = D / 64;            // 64-column (128-byte) chunks of a row
     static constexpr int kRegionBytes = kTN * 128;    // one chunk of a 64-key tile
     static constexpr int kStageBytes = 2 * kChunks * kRegionBytes;  // K chunks then V chunks
-    static constexpr int kStages = D == 128 ? 5 : 8;
+    static constexpr int kStages = D == 128 ? 4 : 6;
+    static constexpr int kPBytes = 128 * kTN * 2;     // P of one half, bf16 [128 rows][64 keys]
+    static constexpr int kPOffset = kStages * kStageBytes;  // P[half][buffer]
     static constexpr int kQCols = D / 2;  // bf16 pairs per row
     __host__ __device__ static constexpr uint32_t colQ(int h) { return h * kQCols; }
     __host__ __device__ static constexpr uint32_t colS(int h) { return 2 * kQCols + h * kTN; }
     __host__ __device__ static constexpr uint32_t colO(int h) { return 2 * kQCols + 2 * kTN + h * D; }
-    // instruction descriptors (kind::f16): D fp32, A/B bf16, M=128
+    // instruction descriptors (kind::f16): D fp32, A/B bf16, M=128.  S = Q K^T: A in
+    // TMEM, B = K tile K-major, N=64.  O += P V: A = P K-major, B = V MN-major, N=d.
     static constexpr uint32_t kIdescQK = (1u << 4) | (1u << 7) | (1u << 10) |
                                          (uint32_t(kTN >> 3) << 17) | (uint32_t(128 >> 4) << 24);
     static constexpr uint32_t kIdescPV = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
                                          (uint32_t(D >> 3) << 17) | (uint32_t(128 >> 4) << 24);
-    // barriers: full[S] empty[S] s_full[2] p_full[2] pv_done[2] q_ready[2] wg_bar[2] fin
-    static constexpr int kNumBars = 2 * kStages + 11;
-    static constexpr int kBarOffset = kStages * kStageBytes;
-    static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;  // tmem base, err, last[2]
+    // barriers: full[S] empty[S] s_full[2] s_free[2] p_full[2][2] pv_done[2][2]
+    //           q_ready[2] fin[2] (1 spare)
+    static constexpr int kNumBars = 2 * kStages + 17;
+    static constexpr int kBarOffset = kPOffset + 4 * kPBytes;
+    static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;  // tmem base, err
     static constexpr int kPrefixOffset = kMiscOffset + 16;
     static constexpr int smem_bytes(int npairs) { return 1024 + kPrefixOffset + (npairs + 1) * 4; }
     static_assert(2 * kQCols + 2 * kTN + 2 * D <= kTmemCols, "TMEM budget");
@@ -91,7 +98,7 @@ struct AttnArgs {
     float scale_log2;
     float *part_o;    // [slots][D][256]
     float2 *part_ml;  // [slots][256]
-    unsigned *pair_cnt;  // [npairs][2]
+    int2 *pair_split;  // [npairs]: first and last CTA of each pair's tile range
     int *err_word;
 };
 
@@ -127,10 +134,10 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 }
 
 // Waits for the phase of `parity` to complete.  Gives up (false) when another
-// role has flagged an error or after kWaitLimitNs, flagging `code`.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *err,
-                                       int code) {
-    if (mbar_try(bar, parity)) return true;
+// role has flagged an error or after kWaitLimitNs, flagging `code`.  Thread-level
+// (the TMA producer runs on one thread).
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *err,
+                                            int code) {
     const uint64_t t0 = globaltimer();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try(bar, parity)) return true;
@@ -143,6 +150,35 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
         }
     }
 }
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *err,
+                                          int code) {
+    if (mbar_try(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, err, code);
+}
+// Warp-collective form: every lane of a converged warp calls it and all get the
+// same answer.  Inline, so a wait that is already satisfied costs a few cycles.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *err,
+                                          int code) {
+    if (__any_sync(0xFFFFFFFFu, mbar_try(bar, parity))) return true;
+    uint64_t t0 = 0;
+    for (uint32_t i = 1;; ++i) {
+        if (__any_sync(0xFFFFFFFFu, mbar_try(bar, parity))) return true;
+        if ((i & 255) == 0) {
+            int stop = 0;
+            if ((threadIdx.x & 31) == 0) {
+                const uint64_t now = globaltimer();
+                if (t0 == 0) t0 = now;
+                if (*err) {
+                    stop = 1;
+                } else if (now - t0 > kWaitLimitNs) {
+                    atomicCAS(const_cast<int *>(err), 0, code);
+                    stop = 1;
+                }
+            }
+            if (__shfl_sync(0xFFFFFFFFu, stop, 0)) return false;
+        }
+    }
+}
 // Bounded wait that ignores the error flag (used to drain copies in flight).
 __device__ __noinline__ bool mbar_drain(uint32_t bar, uint32_t parity) {
     const uint64_t t0 = globaltimer();
@@ -151,13 +187,22 @@ __device__ __noinline__ bool mbar_drain(uint32_t bar, uint32_t parity) {
     return true;
 }
 
+// TMA tile load; `policy` is an L2 cache policy (createpolicy).
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
-                                            int c2, int c3, uint32_t bar) {
+                                            int c2, int c3, uint32_t bar, uint64_t policy) {
     asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar),
+        "l"(policy)
         : "memory");
+}
+// K/V tiles are read once: mark them first in line for eviction from L2 so they do
+// not push out the partials that the merging CTAs read back.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -166,19 +211,34 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     bar)
-                 : "memory");
-}
-// D[tmem] (+)= A[tmem] * B[smem desc]
-__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate) {
+// Warp-converged issue: every lane of the MMA warp executes these, one elected
+// lane (the same one each time) issues the instruction.
+__device__ __forceinline__ void tc_mma_ts_e(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p, e;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void tc_mma_ss_e(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void tc_commit_e(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n" ::"r"(
+            bar)
         : "memory");
 }
 // Shared-memory matrix descriptor, 128-byte swizzle (sm_100 format, version 1).
@@ -233,6 +293,65 @@ __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- softmax arithmetic
+// Packed fp32 pairs (sm_100 f32x2 instructions) and a 3-input maximum.
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void upk2(uint64_t r, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Row maximum of 64 raw scores (bit patterns in v).
+__device__ __forceinline__ float tile_max(const uint32_t *v) {
+    float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int j = 0; j < kTN; j += 8) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            m[q] = fmax3(m[q], __uint_as_float(v[j + 2 * q]), __uint_as_float(v[j + 2 * q + 1]));
+    }
+    return fmax3(m[0], m[1], fmaxf(m[2], m[3]));
+}
+
+// P = 2^(x * c - m) for 64 scores: packed into bf16 pairs (pk), fp32 sum returned.
+__device__ __forceinline__ float exp_tile(const uint32_t *v, float c, float m, uint32_t *pk) {
+    const uint64_t cc = pk2(c, c), nm = pk2(-m, -m);
+    uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+    for (int j = 0; j < kTN / 2; ++j) {
+        const uint64_t y = ffma2(pk2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])), cc, nm);
+        float y0, y1;
+        upk2(y, y0, y1);
+        const uint64_t p = pk2(ex2_approx(y0), ex2_approx(y1));
+        acc[j & 3] = fadd2(acc[j & 3], p);
+        float p0, p1;
+        upk2(p, p0, p1);
+        pk[j] = pack_bf16x2(p0, p1);
+    }
+    const uint64_t s = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+    float s0, s1;
+    upk2(s, s0, s1);
+    return s0 + s1;
+}
+
 // ---------------------------------------------------------------- scheduling
 struct Seg {
     int p, b, g, rg, L, nctx, rows, nh, tile0, ntiles, c_first, c_last;
@@ -247,32 +366,38 @@ struct Sched {
     int P;
     int64_t T, tcur, tend;
 
+    // Next segment of this CTA's range.  Units [prefix[p], prefix[p] + kSegCost) of a
+    // pair carry no work; a range that holds only such units of a pair skips it.
     __device__ bool next(const AttnArgs &a, Seg &s) {
-        if (tcur >= tend) return false;
-        int lo = 0, hi = a.npairs;  // prefix[lo] <= tcur < prefix[hi]
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (prefix[mid] <= tcur) lo = mid; else hi = mid;
+        while (tcur < tend) {
+            int lo = 0, hi = a.npairs;  // prefix[lo] <= tcur < prefix[hi]
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (prefix[mid] <= tcur) lo = mid; else hi = mid;
+            }
+            const int p = lo;
+            const int64_t rs = prefix[p] + kSegCost, pe = prefix[p + 1];
+            const int64_t t0 = tcur > rs ? tcur : rs;
+            const int64_t seg_end = pe < tend ? pe : tend;
+            tcur = seg_end;
+            if (t0 >= seg_end) continue;
+            s.p = p;
+            s.rg = p % a.NRG;
+            const int bg = p / a.NRG;
+            s.g = bg % a.Hkv;
+            s.b = bg / a.Hkv;
+            int L = a.lens[s.b];
+            s.L = L < 0 ? 0 : (L > a.Lmax ? a.Lmax : L);
+            s.nctx = (s.L + kTN - 1) / kTN;
+            s.rows = min(kRows, a.R - s.rg * kRows);
+            s.nh = s.rows > 128 ? 2 : 1;
+            s.tile0 = static_cast<int>(t0 - rs);
+            s.ntiles = static_cast<int>(seg_end - t0);
+            s.c_first = owner_of(rs, P, T);
+            s.c_last = owner_of(pe - 1, P, T);
+            return true;
         }
-        const int p = lo;
-        const int64_t ps = prefix[p], pe = prefix[p + 1];
-        const int64_t seg_end = pe < tend ? pe : tend;
-        s.p = p;
-        s.rg = p % a.NRG;
-        const int bg = p / a.NRG;
-        s.g = bg % a.Hkv;
-        s.b = bg / a.Hkv;
-        int L = a.lens[s.b];
-        s.L = L < 0 ? 0 : (L > a.Lmax ? a.Lmax : L);
-        s.nctx = (s.L + kTN - 1) / kTN;
-        s.rows = min(kRows, a.R - s.rg * kRows);
-        s.nh = s.rows > 128 ? 2 : 1;
-        s.tile0 = static_cast<int>(tcur - ps);
-        s.ntiles = static_cast<int>(seg_end - tcur);
-        s.c_first = owner_of(ps, P, T);
-        s.c_last = owner_of(pe - 1, P, T);
-        tcur = seg_end;
-        return true;
+        return false;
     }
 };
 
@@ -283,19 +408,20 @@ __device__ __forceinline__ int tile_valid(const AttnArgs &a, const Seg &s, int t
 // ---------------------------------------------------------------- roles
 template <int D>
 struct Smem {
-    uint32_t stages, bars;
+    uint32_t stages, pbuf, bars;
     int *prefix;
     volatile int *err;
-    volatile int *last;
     uint32_t *tmem_slot;
+    static constexpr int S2 = 2 * Cfg<D>::kStages;
     __device__ uint32_t full(int i) const { return bars + 8 * i; }
     __device__ uint32_t empty(int i) const { return bars + 8 * (Cfg<D>::kStages + i); }
-    __device__ uint32_t s_full(int h) const { return bars + 8 * (2 * Cfg<D>::kStages + h); }
-    __device__ uint32_t p_full(int h) const { return bars + 8 * (2 * Cfg<D>::kStages + 2 + h); }
-    __device__ uint32_t pv_done(int h) const { return bars + 8 * (2 * Cfg<D>::kStages + 4 + h); }
-    __device__ uint32_t q_ready(int h) const { return bars + 8 * (2 * Cfg<D>::kStages + 6 + h); }
-    __device__ uint32_t wg_bar(int h) const { return bars + 8 * (2 * Cfg<D>::kStages + 8 + h); }
-    __device__ uint32_t fin() const { return bars + 8 * (2 * Cfg<D>::kStages + 10); }
+    __device__ uint32_t s_full(int h) const { return bars + 8 * (S2 + h); }
+    __device__ uint32_t s_free(int h) const { return bars + 8 * (S2 + 2 + h); }
+    __device__ uint32_t p_full(int h, int b) const { return bars + 8 * (S2 + 4 + 2 * h + b); }
+    __device__ uint32_t pv_done(int h, int b) const { return bars + 8 * (S2 + 8 + 2 * h + b); }
+    __device__ uint32_t q_ready(int h) const { return bars + 8 * (S2 + 12 + h); }
+    __device__ uint32_t fin(int h) const { return bars + 8 * (S2 + 14 + h); }
+    __device__ uint32_t p_tile(int h, int b) const { return pbuf + (2 * h + b) * Cfg<D>::kPBytes; }
 };
 
 template <int D>
@@ -305,6 +431,7 @@ __device__ void role_producer(const AttnArgs &a, Sched sch, const Smem<D> &sm,
     using C = Cfg<D>;
     int stage = 0;
     uint32_t phase = 0, issued = 0, last_par = 0;
+    const uint64_t policy = l2_evict_first();
     Seg s;
     bool ok = true;
     while (ok && sch.next(a, s)) {
@@ -321,8 +448,9 @@ __device__ void role_producer(const AttnArgs &a, Sched sch, const Smem<D> &sm,
             const uint32_t sb = sm.stages + stage * C::kStageBytes;
 #pragma unroll
             for (int c = 0; c < C::kChunks; ++c) {
-                tma_load_4d(sb + c * C::kRegionBytes, mk, c * 64, c1, c2, s.b, full);
-                tma_load_4d(sb + (C::kChunks + c) * C::kRegionBytes, mv, c * 64, c1, c2, s.b, full);
+                tma_load_4d(sb + c * C::kRegionBytes, mk, c * 64, c1, c2, s.b, full, policy);
+                tma_load_4d(sb + (C::kChunks + c) * C::kRegionBytes, mv, c * 64, c1, c2, s.b, full,
+                            policy);
             }
             issued |= 1u << stage;
             last_par = (last_par & ~(1u << stage)) | (phase << stage);
@@ -334,85 +462,96 @@ __device__ void role_producer(const AttnArgs &a, Sched sch, const Smem<D> &sm,
         if (issued >> st & 1u) mbar_drain(sm.full(st), last_par >> st & 1u);
 }
 
+// MMA warp of half h (warp 9 + h).  It runs one tile ahead on Q K^T: at step it it
+// issues S_h = Q_h K^T for tile it (once the softmax has read S_h of tile it-1)
+// and then O_h += P_h V for tile it-1 (once its P is in shared memory), so the
+// tensor core computes the next scores while the softmax warps work on the current
+// ones.  The two halves run independently; a K/V stage is released when both MMA
+// warps have finished with it (empty barrier of count 2).
 template <int D>
-__device__ void role_mma(const AttnArgs &a, Sched sch, const Smem<D> &sm, uint32_t tmem) {
+__device__ void role_mma(const AttnArgs &a, Sched sch, const Smem<D> &sm, uint32_t tmem, int h) {
     using C = Cfg<D>;
     const int lane = threadIdx.x & 31;
-    auto wait = [&](uint32_t bar, uint32_t par) -> bool {
-        int ok = 1;
-        if (lane == 0) ok = mbar_wait(bar, par, sm.err, 2);
-        return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
-    };
-    int stage = 0;
-    uint32_t phase = 0, qpar[2] = {0, 0}, ppar[2] = {0, 0}, pv_cnt[2] = {0, 0};
+    auto wait = [&](uint32_t bar, uint32_t par) -> bool { return warp_wait(bar, par, sm.err, 2); };
+    // descriptor bases; a descriptor moves by (byte offset >> 4) in its address field
+    const uint64_t kdesc0 = sdesc_sw128(sm.stages, 16, 1024);
+    const uint64_t vdesc0 =
+        sdesc_sw128(sm.stages + C::kChunks * C::kRegionBytes, C::kRegionBytes, 1024);
+    const uint64_t pdesc0 = sdesc_sw128(sm.pbuf, 16, 1024) + (((2 * h) * C::kPBytes) >> 4);
+    const uint32_t d_s = tmem + C::colS(h), d_o = tmem + C::colO(h), a_q = tmem + C::colQ(h);
+    int stage = 0, prev_stage = 0;
+    uint32_t phase = 0, qpar = 0, s_cnt = 0, p_cnt = 0;
     bool ok = true;
     Seg s;
     while (ok && sch.next(a, s)) {
-        for (int it = 0; it < s.ntiles && ok; ++it) {
-            const int nvalid = tile_valid(a, s, s.tile0 + it);
-            if (!wait(sm.full(stage), phase)) { ok = false; break; }
-            const uint32_t sb = sm.stages + stage * C::kStageBytes;
-            const uint32_t vb = sb + C::kChunks * C::kRegionBytes;
-            for (int h = 0; h < s.nh && ok; ++h) {
+        if (h >= s.nh) {  // half unused in this segment: release each stage at once
+            for (int it = 0; it < s.ntiles; ++it) {
+                if (!wait(sm.full(stage), phase)) { ok = false; break; }
+                if (lane == 0) mbar_arrive(sm.empty(stage));
+                if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+            }
+            continue;
+        }
+        for (int it = 0; it <= s.ntiles && ok; ++it) {
+            if (it < s.ntiles) {
+                const int nvalid = tile_valid(a, s, s.tile0 + it);
+                if (!wait(sm.full(stage), phase)) { ok = false; break; }
+                if (nvalid < kTN) {
+                    // V rows past the valid keys may hold anything (rows >= L_b of the
+                    // cache); P is 0 there, and 0 * NaN must not reach O: zero them
+                    // (both MMA warps write the same zeros before their own P V).
+                    const uint32_t vb = sm.stages + stage * C::kStageBytes +
+                                        C::kChunks * C::kRegionBytes;
+#pragma unroll
+                    for (int c = 0; c < C::kChunks; ++c)
+                        for (uint32_t off = nvalid * 128 + lane * 16; off < C::kRegionBytes;
+                             off += 512)
+                            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(
+                                             vb + c * C::kRegionBytes + off),
+                                         "r"(0u)
+                                         : "memory");
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                }
                 if (it == 0) {
-                    if (!wait(sm.q_ready(h), qpar[h])) { ok = false; break; }
-                    qpar[h] ^= 1;
+                    if (!wait(sm.q_ready(h), qpar)) { ok = false; break; }
+                    qpar ^= 1;
                 }
-                // S_h and P_h share columns: the previous P_h V must be done reading
-                if (pv_cnt[h] > 0 && !wait(sm.pv_done(h), (pv_cnt[h] - 1) & 1)) { ok = false; break; }
+                // S_h is free once the softmax has read the previous one
+                if (s_cnt > 0 && !wait(sm.s_free(h), (s_cnt - 1) & 1)) { ok = false; break; }
                 tc_fence_after();
-                if (lane == 0) {
+                const uint64_t kd = kdesc0 + ((stage * C::kStageBytes) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t addr = sb + (kk >> 2) * C::kRegionBytes + (kk & 3) * 32;
-                        tc_mma_ts(tmem + C::colS(h), tmem + C::colQ(h) + kk * 8,
-                                  sdesc_sw128(addr, 16, 1024), C::kIdescQK, kk > 0);
-                    }
-                    tc_commit(sm.s_full(h));
-                }
-                __syncwarp();
+                for (int kk = 0; kk < D / 16; ++kk)
+                    tc_mma_ts_e(d_s, a_q + kk * 8,
+                                kd + (((kk >> 2) * C::kRegionBytes + (kk & 3) * 32) >> 4),
+                                C::kIdescQK, kk > 0);
+                tc_commit_e(sm.s_full(h));
+                ++s_cnt;
             }
-            if (!ok) break;
-            if (nvalid < kTN) {
-                // V rows past the valid keys may hold anything (rows >= L_b of the
-                // cache); P is 0 there, and 0 * NaN must not reach O: zero them.
-#pragma unroll
-                for (int c = 0; c < C::kChunks; ++c) {
-                    const uint32_t base = vb + c * C::kRegionBytes;
-                    for (uint32_t off = nvalid * 128 + lane * 16; off < C::kRegionBytes; off += 512)
-                        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(base + off),
-                                     "r"(0u)
-                                     : "memory");
-                }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
-            }
-            for (int h = 0; h < s.nh && ok; ++h) {
-                if (!wait(sm.p_full(h), ppar[h])) { ok = false; break; }
-                ppar[h] ^= 1;
+            if (it > 0) {  // O_h += P_h V for the previous tile
+                const uint32_t b = p_cnt & 1;
+                if (!wait(sm.p_full(h, b), (p_cnt >> 1) & 1)) { ok = false; break; }
                 tc_fence_after();
-                if (lane == 0) {
+                const uint64_t vd = vdesc0 + ((prev_stage * C::kStageBytes) >> 4);
+                const uint64_t pd = pdesc0 + ((b * C::kPBytes) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < kTN / 16; ++kk)
-                        tc_mma_ts(tmem + C::colO(h), tmem + C::colS(h) + kk * 8,
-                                  sdesc_sw128(vb + kk * 2048, C::kRegionBytes, 1024), C::kIdescPV,
-                                  (it > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(sm.pv_done(h));
-                }
-                __syncwarp();
-                ++pv_cnt[h];
+                for (int kk = 0; kk < kTN / 16; ++kk)
+                    tc_mma_ss_e(d_o, pd + ((kk * 32) >> 4), vd + ((kk * 2048) >> 4), C::kIdescPV,
+                                (it > 1 || kk > 0) ? 1u : 0u);
+                tc_commit_e(sm.pv_done(h, b));
+                ++p_cnt;
+                tc_commit_e(sm.empty(prev_stage));
             }
-            if (!ok) break;
-            if (lane == 0) tc_commit(sm.empty(stage));
-            __syncwarp();
-            if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+            if (it < s.ntiles) {
+                prev_stage = stage;
+                if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+            }
         }
     }
     // every MMA issued here completes before TMEM is freed
-    if (lane == 0) {
-        tc_commit(sm.fin());
-        mbar_drain(sm.fin(), 0);
-    }
+    tc_commit_e(sm.fin(h));
+    if (lane == 0) mbar_drain(sm.fin(h), 0);
     __syncwarp();
 }
 
@@ -448,18 +587,12 @@ __device__ void role_softmax(const AttnArgs &a, Sched sch, const Smem<D> &sm, ui
     const int h = warp >> 2, q4 = warp & 3, r = q4 * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(q4 * 32) << 16);  // this warp's lanes
     const float c = a.scale_log2;
-    auto wait = [&](uint32_t bar, uint32_t par) -> bool {
-        int ok = 1;
-        if (lane == 0) ok = mbar_wait(bar, par, sm.err, 3);
-        return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
-    };
-    uint32_t spar = 0, pv_seen = 0, wgpar = 0;
-    auto wg_sync = [&]() -> bool {
-        mbar_arrive(sm.wg_bar(h));
-        const bool ok = wait(sm.wg_bar(h), wgpar);
-        wgpar ^= 1;
-        return ok;
-    };
+    auto wait = [&](uint32_t bar, uint32_t par) -> bool { return warp_wait(bar, par, sm.err, 3); };
+    // O_h += P_h V of this half's tile number n has completed
+    auto wait_pv = [&](uint32_t n) -> bool { return wait(sm.pv_done(h, n & 1), (n >> 1) & 1); };
+    uint32_t spar = 0, cnt = 0;  // cnt: tiles of this half so far
+    // this thread's P row inside a [128][64] bf16 tile, 128-byte swizzle
+    const uint32_t prow = (r >> 3) * 1024 + (r & 7) * 128;
     bool ok = true;
     Seg s;
     while (ok && sch.next(a, s)) {
@@ -499,20 +632,28 @@ __device__ void role_softmax(const AttnArgs &a, Sched sch, const Smem<D> &sm, ui
             tmem_ld32(tl + C::colS(h) + 32, v + 32);
             tmem_wait_ld(v);
             tmem_touch(v + 32);
-            float mx = -INFINITY;
+            tc_fence_before();
+            mbar_arrive(sm.s_free(h));  // the MMA warp may overwrite S_h now
+            if (nvalid < kTN) {
 #pragma unroll
-            for (int j = 0; j < kTN; ++j) {
-                float x = __uint_as_float(v[j]);
-                if (nvalid < kTN && j >= nvalid) x = -INFINITY;
-                v[j] = __float_as_uint(x);
-                mx = fmaxf(mx, x);
+                for (int j = 0; j < kTN; ++j)
+                    if (j >= nvalid) v[j] = __float_as_uint(-INFINITY);
             }
-            const float m_tile = mx * c;
-            if (it == 0) {
-                m_run = m_tile;
-            } else {
+            // The running max m_run (log2 units) is raised only when a tile's max exceeds
+            // it by more than kRescaleLog2; otherwise P is taken against the stale max,
+            // which leaves O / l unchanged (both carry the same factor) and lets the
+            // exponentials start without waiting for this tile's max.
+            const float mx = tile_max(v);
+            if (it == 0) m_run = mx * c;
+            uint32_t pk[kTN / 2];
+            float lsum = exp_tile(v, c, m_run, pk);
+            if (it > 0) {
+                const float m_tile = mx * c;
                 const bool need = m_tile > m_run + kRescaleLog2;
                 if (__any_sync(0xFFFFFFFFu, need)) {
+                    // O_h must hold every earlier tile before it is rescaled
+                    if (!wait_pv(cnt - 1)) { ok = false; break; }
+                    tc_fence_after();
                     const float f = need ? ex2_approx(m_run - m_tile) : 1.f;
                     if (need) { l_run *= f; m_run = m_tile; }
 #pragma unroll 1
@@ -525,28 +666,28 @@ __device__ void role_softmax(const AttnArgs &a, Sched sch, const Smem<D> &sm, ui
                         tmem_st32(tl + C::colO(h) + 32 * j, o);
                     }
                     tmem_wait_st();
+                    lsum = exp_tile(v, c, m_run, pk);
                 }
             }
-            const float neg_m = -m_run;
-            float sum = 0.f;
-            uint32_t pk[kTN / 2];
+            l_run += lsum;
+            // the P buffer of this tile was last read by the P V two tiles back
+            if (cnt >= 2 && !wait_pv(cnt - 2)) { ok = false; break; }
+            const uint32_t pt = sm.p_tile(h, cnt & 1) + prow;
 #pragma unroll
-            for (int j = 0; j < kTN / 2; ++j) {
-                const float p0 = ex2_approx(fmaf(__uint_as_float(v[2 * j]), c, neg_m));
-                const float p1 = ex2_approx(fmaf(__uint_as_float(v[2 * j + 1]), c, neg_m));
-                sum += p0 + p1;
-                pk[j] = pack_bf16x2(p0, p1);
-            }
-            l_run += sum;
-            tmem_st32(tl + C::colS(h), pk);
-            tmem_wait_st();
+            for (int ch = 0; ch < 8; ++ch)
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                 pt + ((ch ^ (r & 7)) << 4)),
+                             "r"(pk[4 * ch]), "r"(pk[4 * ch + 1]), "r"(pk[4 * ch + 2]),
+                             "r"(pk[4 * ch + 3])
+                             : "memory");
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             tc_fence_before();
-            mbar_arrive(sm.p_full(h));
-            ++pv_seen;
+            mbar_arrive(sm.p_full(h, cnt & 1));
+            ++cnt;
         }
         if (!ok) break;
         // ---- segment epilogue: O_h is final once the last P_h V is done
-        if (!wait(sm.pv_done(h), (pv_seen - 1) & 1)) { ok = false; break; }
+        if (!wait_pv(cnt - 1)) { ok = false; break; }
         tc_fence_after();
         if (s.c_first == s.c_last) {
             const float inv = 1.f / l_run;
@@ -565,7 +706,7 @@ __device__ void role_softmax(const AttnArgs &a, Sched sch, const Smem<D> &sm, ui
             if (valid) store_lse(a, s, rl, m_run, l_run);
             continue;
         }
-        // ---- split pair: write this CTA's partial, the last CTA to arrive merges
+        // ---- split pair: write this CTA's partial; block_attn_merge_kernel combines them
         const int cta = blockIdx.x;
         const size_t slot = static_cast<size_t>(cta + s.p);
 #pragma unroll 1
@@ -580,44 +721,9 @@ __device__ void role_softmax(const AttnArgs &a, Sched sch, const Smem<D> &sm, ui
             }
         }
         if (valid) __stcg(a.part_ml + slot * kRows + rl, make_float2(m_run, l_run));
-        __threadfence();
-        if (!wg_sync()) { ok = false; break; }
-        if (r == 0) {
-            const unsigned old = atomicAdd(a.pair_cnt + 2 * s.p + h, 1u);
-            sm.last[h] = old == static_cast<unsigned>(s.c_last - s.c_first);
-        }
-        if (!wg_sync()) { ok = false; break; }
-        if (!sm.last[h]) continue;
-        __threadfence();
-        if (valid) {
-            float M = -INFINITY;
-            for (int cc = s.c_first; cc <= s.c_last; ++cc)
-                M = fmaxf(M, __ldcg(a.part_ml + static_cast<size_t>(cc + s.p) * kRows + rl).x);
-            float den = 0.f;
-            for (int cc = s.c_first; cc <= s.c_last; ++cc) {
-                const float2 ml = __ldcg(a.part_ml + static_cast<size_t>(cc + s.p) * kRows + rl);
-                den += ex2_approx(ml.x - M) * ml.y;
-            }
-            const float inv = 1.f / den;
-#pragma unroll 1
-            for (int j = 0; j < D / 32; ++j) {
-                float acc[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-                for (int cc = s.c_first; cc <= s.c_last; ++cc) {
-                    const size_t sl = static_cast<size_t>(cc + s.p);
-                    const float w = ex2_approx(__ldcg(a.part_ml + sl * kRows + rl).x - M) * inv;
-                    const float *src = a.part_o + (sl * D + 32 * j) * kRows + rl;
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) acc[e] += w * __ldcg(src + e * kRows);
-                }
-                store_row<D>(a, s, rl, acc, 32 * j);
-            }
-            store_lse(a, s, rl, M, den);
-        }
-        if (r == 0) a.pair_cnt[2 * s.p + h] = 0u;
     }
 }
+
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -644,7 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int p = p0; p < p1; ++p) {
             int L = a.lens[p / (a.Hkv * a.NRG)];
             L = L < 0 ? 0 : (L > a.Lmax ? a.Lmax : L);
-            local += (L + kTN - 1) / kTN + 1;
+            local += (L + kTN - 1) / kTN + 1 + kSegCost;
         }
         int incl = local;
 #pragma unroll
@@ -669,7 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefix[p] = run;
             int L = a.lens[p / (a.Hkv * a.NRG)];
             L = L < 0 ? 0 : (L > a.Lmax ? a.Lmax : L);
-            run += (L + kTN - 1) / kTN + 1;
+            run += (L + kTN - 1) / kTN + 1 + kSegCost;
         }
         if (t == kThreads - 1) prefix[a.npairs] = run;
         __syncthreads();
@@ -680,27 +786,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int P = static_cast<int>(parts);
     const int cta = blockIdx.x;
     if (cta >= P) return;
+    if (cta == 0)
+        for (int p = t; p < a.npairs; p += kThreads)
+            a.pair_split[p] = make_int2(owner_of(prefix[p] + kSegCost, P, T), owner_of(prefix[p + 1] - 1, P, T));
 
     Smem<D> sm;
     sm.stages = smem_u32(smem);
+    sm.pbuf = smem_u32(smem + C::kPOffset);
     sm.bars = smem_u32(smem + C::kBarOffset);
     sm.prefix = prefix;
     sm.tmem_slot = reinterpret_cast<uint32_t *>(misc);
     sm.err = misc + 1;
-    sm.last = misc + 2;
     if (t == 0) {
         for (int i = 0; i < C::kStages; ++i) {
             mbar_init(sm.full(i), 1);
-            mbar_init(sm.empty(i), 1);
+            mbar_init(sm.empty(i), 2);
         }
         for (int h = 0; h < 2; ++h) {
             mbar_init(sm.s_full(h), 1);
-            mbar_init(sm.p_full(h), 128);
-            mbar_init(sm.pv_done(h), 1);
+            mbar_init(sm.s_free(h), 128);
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(sm.p_full(h, b), 128);
+                mbar_init(sm.pv_done(h, b), 1);
+            }
             mbar_init(sm.q_ready(h), 128);
-            mbar_init(sm.wg_bar(h), 128);
         }
-        mbar_init(sm.fin(), 1);
+        mbar_init(sm.fin(0), 1);
+        mbar_init(sm.fin(1), 1);
         *sm.err = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -726,8 +838,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducerWarp) {
         if (lane == 0) role_producer<D>(a, sch, sm, &tm_kc, &tm_vc, &tm_kb, &tm_vb);
         __syncwarp();
-    } else if (warp == kMmaWarp) {
-        role_mma<D>(a, sch, sm, tmem);
+    } else if (warp >= kMmaWarp) {
+        role_mma<D>(a, sch, sm, tmem, warp - kMmaWarp);
     } else {
         role_softmax<D>(a, sch, sm, tmem);
     }
@@ -740,6 +852,86 @@ __global__ void __launch_bounds__(kThreads, 1)
                      "r"(kTmemCols)
                      : "memory");
     if (t == 0 && *sm.err) atomicOr(a.err_word, *sm.err);
+}
+
+// Combines the partials of every pair whose tiles were split across CTAs:
+//   M = max_c m_c,  out = sum_c 2^(m_c-M) O_c / sum_c 2^(m_c-M) l_c,
+//   lse = (M + log2 sum_c 2^(m_c-M) l_c) ln 2.
+// Block (pair p, 32-row chunk of the pair's 256 rows), 8 warps; warp w owns d/8
+// columns and lane i row i of the chunk, so every load of a partial is a coalesced
+// 128-byte line, and the partial loop is unrolled to keep many lines in flight.
+constexpr int kMergeThreads = 256;
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads) block_attn_merge_kernel(const AttnArgs a) {
+    constexpr int kCols = D / 8;
+    const int p = blockIdx.x >> 3, chunk = blockIdx.x & 7;
+    const int2 cs = a.pair_split[p];
+    if (cs.x == cs.y) return;  // finished inside one CTA
+    const int rg = p % a.NRG;
+    const int rows = min(kRows, a.R - rg * kRows);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int rl = chunk * 32 + lane;
+    if (rl >= rows) return;
+    const float2 *ml_base = a.part_ml + static_cast<size_t>(p) * kRows + rl;  // + c * kRows
+    // partials are read in batches of kBatch with every load of a batch issued
+    // before any is used, so a batch costs one L2 round trip
+    constexpr int kBatch = 8;
+    float M = -INFINITY;
+    for (int c0 = cs.x; c0 <= cs.y; c0 += kBatch) {
+        float m[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+            m[u] = c0 + u <= cs.y ? __ldcg(ml_base + static_cast<size_t>(c0 + u) * kRows).x
+                                  : -INFINITY;
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) M = fmaxf(M, m[u]);
+    }
+    float den = 0.f;
+    float acc[kCols];
+#pragma unroll
+    for (int e = 0; e < kCols; ++e) acc[e] = 0.f;
+    for (int c0 = cs.x; c0 <= cs.y; c0 += kBatch) {
+        float2 ml[kBatch];
+        float v[kBatch][kCols];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int c = c0 + u;
+            if (c <= cs.y) {
+                ml[u] = __ldcg(ml_base + static_cast<size_t>(c) * kRows);
+                const float *src =
+                    a.part_o + (static_cast<size_t>(c + p) * D + kCols * warp) * kRows + rl;
+#pragma unroll
+                for (int e = 0; e < kCols; ++e) v[u][e] = __ldcg(src + e * kRows);
+            } else {
+                ml[u] = make_float2(-INFINITY, 0.f);
+#pragma unroll
+                for (int e = 0; e < kCols; ++e) v[u][e] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const float w = ex2_approx(ml[u].x - M);
+            den += w * ml[u].y;
+#pragma unroll
+            for (int e = 0; e < kCols; ++e) acc[e] += w * v[u][e];
+        }
+    }
+    const float inv = 1.f / den;
+    const int rr = rg * kRows + rl;
+    const int bg = p / a.NRG, g = bg % a.Hkv, b = bg / a.Hkv;
+    const int sq = rr / a.G, head = g * a.G + rr % a.G;
+    uint16_t *dst = a.out + b * a.os[0] + sq * a.os[1] + head * a.os[2] + kCols * warp;
+#pragma unroll
+    for (int j = 0; j < kCols / 8; ++j) {
+        uint4 o;
+        o.x = pack_bf16x2(acc[8 * j + 0] * inv, acc[8 * j + 1] * inv);
+        o.y = pack_bf16x2(acc[8 * j + 2] * inv, acc[8 * j + 3] * inv);
+        o.z = pack_bf16x2(acc[8 * j + 4] * inv, acc[8 * j + 5] * inv);
+        o.w = pack_bf16x2(acc[8 * j + 6] * inv, acc[8 * j + 7] * inv);
+        *reinterpret_cast<uint4 *>(dst + 8 * j) = o;
+    }
+    if (warp == 0 && a.lse)
+        a.lse[(static_cast<int64_t>(b) * a.Hq + head) * a.S + sq] = (M + __log2f(den)) * kLn2;
 }
 
 // ---------------------------------------------------------------- host
@@ -772,7 +964,7 @@ tt_status validate(const tt_attn_desc *d, Geometry *geo, const char *fn) {
     if (np > kMaxPairs)
         return fail(TT_ERR_UNSUPPORTED, "%s: B*Hkv*ceil(S*Hq/Hkv/256) = %lld > %d", fn,
                     (long long)np, kMaxPairs);
-    if (np * ((static_cast<int64_t>(d->Lmax) + kTN - 1) / kTN + 1) >= (int64_t(1) << 31))
+    if (np * ((static_cast<int64_t>(d->Lmax) + kTN - 1) / kTN + 1 + kSegCost) >= (int64_t(1) << 31))
         return fail(TT_ERR_UNSUPPORTED, "%s: more than 2^31 key tiles", fn);
     geo->npairs = static_cast<int>(np);
     geo->P = sm_count();
@@ -782,7 +974,7 @@ tt_status validate(const tt_attn_desc *d, Geometry *geo, const char *fn) {
 
 struct AttnWs {
     int *err_word;
-    unsigned *pair_cnt;
+    int2 *pair_split;
     float2 *part_ml;
     float *part_o;
     size_t bytes;
@@ -792,7 +984,7 @@ AttnWs carve(void *base, int npairs, size_t slots, int d) {
     Carve c(base);
     AttnWs w;
     w.err_word = c.take<int>(1);
-    w.pair_cnt = c.take<unsigned>(2 * static_cast<size_t>(npairs));
+    w.pair_split = c.take<int2>(static_cast<size_t>(npairs));
     w.part_ml = c.take<float2>(slots * kRows);
     w.part_o = c.take<float>(slots * kRows * d);
     w.bytes = c.bytes();
@@ -880,7 +1072,10 @@ tt_status launch(const tt_attn_desc *d, const AttnArgs &a, const void *k_ctx, co
     }
     block_attn_tc_kernel<D><<<a.P, kThreads, Cfg<D>::smem_bytes(a.npairs), stream>>>(kc, vc, kb,
                                                                                     vb, a);
-    return cuda_status(cudaGetLastError(), "tt_block_attn launch");
+    tt_status st2 = cuda_status(cudaGetLastError(), "tt_block_attn launch");
+    if (st2 != TT_OK) return st2;
+    block_attn_merge_kernel<D><<<a.npairs * 8, kMergeThreads, 0, stream>>>(a);
+    return cuda_status(cudaGetLastError(), "tt_block_attn merge launch");
 }
 
 tt_status check_ptrs(const tt_attn_desc *d, const void *q, const void *k_ctx, const void *v_ctx,
@@ -923,7 +1118,7 @@ tt_status run(const tt_attn_desc *d, const Geometry &g, const AttnWs &w, const v
     a.scale_log2 = static_cast<float>(scale * 1.4426950408889634);
     a.part_o = w.part_o;
     a.part_ml = w.part_ml;
-    a.pair_cnt = w.pair_cnt;
+    a.pair_split = w.pair_split;
     a.err_word = w.err_word;
     if (d->d == 128) return launch<128>(d, a, k_ctx, v_ctx, k_blk, v_blk, stream, fn);
     return launch<64>(d, a, k_ctx, v_ctx, k_blk, v_blk, stream, fn);
