@@ -17,9 +17,9 @@
 //    per CTA (P = min(#SMs, tiles/4)); a CTA walks its range segment by segment
 //    (a segment = the part of one pair inside the range);
 //  * a pair whose tiles fall in one CTA is finished there; otherwise each CTA
-//    writes an fp32 partial (O, running max m, sum l) and the last CTA to arrive
-//    (per pair and half) merges them: M = max m_c,
-//    O = sum 2^(m_c-M) O_c / sum 2^(m_c-M) l_c.  No CTA waits on another.
+//    writes an fp32 partial (O / l, running max m, sum l) and a second kernel,
+//    launched as a programmatic dependent, merges them: M = max m_c,
+//    O = sum 2^(m_c-M) l_c O_c / sum 2^(m_c-M) l_c.  No CTA waits on another.
 //
 // Inside a CTA (320 threads, one CTA per SM, 512 TMEM columns):
 //  warp 8     TMA producer: K and V tiles (64 keys x d, 128-byte swizzle) into a
@@ -79,10 +79,10 @@ struct Cfg {
     static constexpr uint32_t kIdescPV = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
                                          (uint32_t(D >> 3) << 17) | (uint32_t(128 >> 4) << 24);
     // barriers: full[S] empty[S] s_full[2] s_free[2] p_full[2][2] pv_done[2][2]
-    //           q_ready[2] fin[2] (1 spare)
-    static constexpr int kNumBars = 2 * kStages + 17;
+    //           q_ready[2] fin[2] wg_bar[2]
+    static constexpr int kNumBars = 2 * kStages + 18;
     static constexpr int kBarOffset = kPOffset + 4 * kPBytes;
-    static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;  // tmem base, err
+    static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;  // tmem base, err, last[2]
     static constexpr int kPrefixOffset = kMiscOffset + 16;
     static constexpr int smem_bytes(int npairs) { return 1024 + kPrefixOffset + (npairs + 1) * 4; }
     static_assert(2 * kQCols + 2 * kTN + 2 * D <= kTmemCols, "TMEM budget");
@@ -96,7 +96,7 @@ struct AttnArgs {
     const int32_t *lens;
     int B, S, Hq, Hkv, G, Lmax, R, NRG, npairs, P;
     float scale_log2;
-    float *part_o;    // [slots][D][256]
+    float *part_o;    // [slots][D][256], O / l of the CTA's tiles
     float2 *part_ml;  // [slots][256]
     int2 *pair_split;  // [npairs]: first and last CTA of each pair's tile range
     int *err_word;
@@ -411,6 +411,7 @@ struct Smem {
     uint32_t stages, pbuf, bars;
     int *prefix;
     volatile int *err;
+    volatile int *last;
     uint32_t *tmem_slot;
     static constexpr int S2 = 2 * Cfg<D>::kStages;
     __device__ uint32_t full(int i) const { return bars + 8 * i; }
@@ -421,6 +422,7 @@ struct Smem {
     __device__ uint32_t pv_done(int h, int b) const { return bars + 8 * (S2 + 8 + 2 * h + b); }
     __device__ uint32_t q_ready(int h) const { return bars + 8 * (S2 + 12 + h); }
     __device__ uint32_t fin(int h) const { return bars + 8 * (S2 + 14 + h); }
+    __device__ uint32_t wg_bar(int h) const { return bars + 8 * (S2 + 16 + h); }
     __device__ uint32_t p_tile(int h, int b) const { return pbuf + (2 * h + b) * Cfg<D>::kPBytes; }
 };
 
@@ -706,9 +708,10 @@ __device__ void role_softmax(const AttnArgs &a, Sched sch, const Smem<D> &sm, ui
             if (valid) store_lse(a, s, rl, m_run, l_run);
             continue;
         }
-        // ---- split pair: write this CTA's partial; block_attn_merge_kernel combines them
-        const int cta = blockIdx.x;
-        const size_t slot = static_cast<size_t>(cta + s.p);
+        // ---- split pair: write this CTA's partial (O / l, m, l); block_attn_merge_kernel
+        // combines the partials once the whole grid has finished
+        const size_t slot = static_cast<size_t>(blockIdx.x + s.p);
+        const float inv = 1.f / l_run;
 #pragma unroll 1
         for (int j = 0; j < D / 32; ++j) {
             uint32_t o[32];
@@ -717,7 +720,7 @@ __device__ void role_softmax(const AttnArgs &a, Sched sch, const Smem<D> &sm, ui
             if (valid) {
                 float *dst = a.part_o + (slot * D + 32 * j) * kRows + rl;
 #pragma unroll
-                for (int e = 0; e < 32; ++e) __stcg(dst + e * kRows, __uint_as_float(o[e]));
+                for (int e = 0; e < 32; ++e) __stcg(dst + e * kRows, __uint_as_float(o[e]) * inv);
             }
         }
         if (valid) __stcg(a.part_ml + slot * kRows + rl, make_float2(m_run, l_run));
@@ -785,10 +788,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     parts = parts < 1 ? 1 : (parts > a.P ? a.P : parts);
     const int P = static_cast<int>(parts);
     const int cta = blockIdx.x;
+    // the merge kernel (programmatic dependent launch) may be scheduled now; it
+    // waits for this grid to finish before it reads anything
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (cta >= P) return;
     if (cta == 0)
         for (int p = t; p < a.npairs; p += kThreads)
-            a.pair_split[p] = make_int2(owner_of(prefix[p] + kSegCost, P, T), owner_of(prefix[p + 1] - 1, P, T));
+            a.pair_split[p] = make_int2(owner_of(prefix[p] + kSegCost, P, T),
+                                        owner_of(prefix[p + 1] - 1, P, T));
 
     Smem<D> sm;
     sm.stages = smem_u32(smem);
@@ -797,6 +804,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     sm.prefix = prefix;
     sm.tmem_slot = reinterpret_cast<uint32_t *>(misc);
     sm.err = misc + 1;
+    sm.last = misc + 2;
     if (t == 0) {
         for (int i = 0; i < C::kStages; ++i) {
             mbar_init(sm.full(i), 1);
@@ -855,15 +863,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Combines the partials of every pair whose tiles were split across CTAs:
-//   M = max_c m_c,  out = sum_c 2^(m_c-M) O_c / sum_c 2^(m_c-M) l_c,
+//   M = max_c m_c,  out = sum_c 2^(m_c-M) l_c (O_c/l_c) / sum_c 2^(m_c-M) l_c,
 //   lse = (M + log2 sum_c 2^(m_c-M) l_c) ln 2.
-// Block (pair p, 32-row chunk of the pair's 256 rows), 8 warps; warp w owns d/8
+// Block = (pair, 32-row chunk of the pair's 256 rows), 8 warps; warp w owns d/8
 // columns and lane i row i of the chunk, so every load of a partial is a coalesced
-// 128-byte line, and the partial loop is unrolled to keep many lines in flight.
+// 128-byte line, and the loads of up to 8 partials are issued before any is used.
+// Launched as a programmatic dependent of the attention kernel: griddepcontrol.wait
+// returns once that grid has completed and its writes are visible.
 constexpr int kMergeThreads = 256;
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) block_attn_merge_kernel(const AttnArgs a) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     constexpr int kCols = D / 8;
+    constexpr int kBatch = 8;
     const int p = blockIdx.x >> 3, chunk = blockIdx.x & 7;
     const int2 cs = a.pair_split[p];
     if (cs.x == cs.y) return;  // finished inside one CTA
@@ -872,21 +884,8 @@ __global__ void __launch_bounds__(kMergeThreads) block_attn_merge_kernel(const A
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int rl = chunk * 32 + lane;
     if (rl >= rows) return;
-    const float2 *ml_base = a.part_ml + static_cast<size_t>(p) * kRows + rl;  // + c * kRows
-    // partials are read in batches of kBatch with every load of a batch issued
-    // before any is used, so a batch costs one L2 round trip
-    constexpr int kBatch = 8;
-    float M = -INFINITY;
-    for (int c0 = cs.x; c0 <= cs.y; c0 += kBatch) {
-        float m[kBatch];
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u)
-            m[u] = c0 + u <= cs.y ? __ldcg(ml_base + static_cast<size_t>(c0 + u) * kRows).x
-                                  : -INFINITY;
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) M = fmaxf(M, m[u]);
-    }
-    float den = 0.f;
+    const float2 *mlp = a.part_ml + static_cast<size_t>(p) * kRows + rl;  // + c * kRows
+    float M = -INFINITY, den = 0.f;
     float acc[kCols];
 #pragma unroll
     for (int e = 0; e < kCols; ++e) acc[e] = 0.f;
@@ -897,7 +896,7 @@ __global__ void __launch_bounds__(kMergeThreads) block_attn_merge_kernel(const A
         for (int u = 0; u < kBatch; ++u) {
             const int c = c0 + u;
             if (c <= cs.y) {
-                ml[u] = __ldcg(ml_base + static_cast<size_t>(c) * kRows);
+                ml[u] = __ldcg(mlp + static_cast<size_t>(c) * kRows);
                 const float *src =
                     a.part_o + (static_cast<size_t>(c + p) * D + kCols * warp) * kRows + rl;
 #pragma unroll
@@ -908,13 +907,21 @@ __global__ void __launch_bounds__(kMergeThreads) block_attn_merge_kernel(const A
                 for (int e = 0; e < kCols; ++e) v[u][e] = 0.f;
             }
         }
+        float Mb = M;
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) Mb = fmaxf(Mb, ml[u].x);
+        const float so = ex2_approx(M - Mb);
+        den *= so;
+#pragma unroll
+        for (int e = 0; e < kCols; ++e) acc[e] *= so;
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
-            const float w = ex2_approx(ml[u].x - M);
-            den += w * ml[u].y;
+            const float w = ex2_approx(ml[u].x - Mb) * ml[u].y;
+            den += w;
 #pragma unroll
             for (int e = 0; e < kCols; ++e) acc[e] += w * v[u][e];
         }
+        M = Mb;
     }
     const float inv = 1.f / den;
     const int rr = rg * kRows + rl;
@@ -1074,8 +1081,18 @@ tt_status launch(const tt_attn_desc *d, const AttnArgs &a, const void *k_ctx, co
                                                                                     vb, a);
     tt_status st2 = cuda_status(cudaGetLastError(), "tt_block_attn launch");
     if (st2 != TT_OK) return st2;
-    block_attn_merge_kernel<D><<<a.npairs * 8, kMergeThreads, 0, stream>>>(a);
-    return cuda_status(cudaGetLastError(), "tt_block_attn merge launch");
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.npairs) * 8);
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaLaunchKernelEx(&cfg, block_attn_merge_kernel<D>, a),
+                       "tt_block_attn merge launch");
 }
 
 tt_status check_ptrs(const tt_attn_desc *d, const void *q, const void *k_ctx, const void *v_ctx,
