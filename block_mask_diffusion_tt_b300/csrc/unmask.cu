@@ -9,9 +9,11 @@
 //  * grid = (B*S rows) x (nch vocabulary chunks), 256 threads per CTA; a CTA
 //    whose row is not masked returns after one arrival (rows that are not masked
 //    cost one byte of traffic);
-//  * one pass over the chunk with 16-byte streaming loads, four in flight per
+//  * one pass over the chunk with 16-byte streaming loads, eight in flight per
 //    thread; per thread a running raw-logit maximum, its first index and
-//    sum 2^((l - max) * log2(e)/T), rescaled when the maximum grows;
+//    sum 2^((l - max) * log2(e)/T), rescaled when the maximum grows; a vector of
+//    8 logits whose maximum lies 2^40 below the running maximum's term adds
+//    nothing and costs no exponentials (bounded below, at kSkipLog2);
 //  * warp-shuffle then shared-memory merge to one partial per CTA; the last CTA
 //    of a row (arrival counter) merges the row's nch partials into (token, conf);
 //  * the last row of a sequence to arrive (counter over all S rows, masked or
@@ -30,7 +32,13 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kMaxS = 64;
-constexpr int kUnroll = 4;
+constexpr int kUnroll = 8;
+// Terms 2^((l - m) k) below 2^-kSkipLog2 of the running maximum's term are not
+// added: a vector of logits whose largest element is that far below the running
+// maximum contributes nothing.  The maximum is only ever raised, so every skipped
+// term is below 2^-kSkipLog2 of the final sum's largest term, and the skipped mass
+// is at most V * 2^-kSkipLog2 of the sum (1.2e-7 relative at V = 131072).
+constexpr float kSkipLog2 = 40.f;
 
 struct UnmaskArgs {
     const char *logits;
@@ -92,12 +100,20 @@ __device__ __forceinline__ void acc_add(Acc &a, float x, int idx, float k) {
     if (a.m != -INFINITY) a.s += ex2_approx((x - a.m) * k);
 }
 
-// Adds n (4 or 8) consecutive elements starting at index idx.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Adds N (4 or 8) consecutive elements starting at index idx.
 template <int N>
 __device__ __forceinline__ void acc_add_vec(Acc &a, const float (&x)[N], int idx, float k) {
-    float lm = x[0];
-#pragma unroll
-    for (int j = 1; j < N; ++j) lm = fmaxf(lm, x[j]);
+    float lm;
+    if constexpr (N == 8)
+        lm = fmax3(fmax3(x[0], x[1], x[2]), fmax3(x[3], x[4], x[5]), fmaxf(x[6], x[7]));
+    else
+        lm = fmax3(x[0], x[1], fmaxf(x[2], x[3]));
     if (lm > a.m) {
         int j0 = N - 1;
 #pragma unroll
@@ -107,7 +123,7 @@ __device__ __forceinline__ void acc_add_vec(Acc &a, const float (&x)[N], int idx
         a.m = lm;
         a.i = idx + j0;
     }
-    if (a.m != -INFINITY) {
+    if (a.m != -INFINITY && (lm - a.m) * k > -kSkipLog2) {
         float s0 = 0.f, s1 = 0.f;
 #pragma unroll
         for (int j = 0; j < N; j += 2) {
@@ -345,7 +361,7 @@ struct Plan {
 };
 
 Plan plan_for(int V) {
-    int nch = (V + 16383) / 16384;
+    int nch = (V + 32767) / 32768;
     if (nch < 1) nch = 1;
     if (nch > 64) nch = 64;
     int chunk = (V + nch - 1) / nch;
