@@ -79,7 +79,7 @@ struct Cfg {
     static constexpr uint32_t kIdescPV = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
                                          (uint32_t(D >> 3) << 17) | (uint32_t(128 >> 4) << 24);
     // barriers: full[S] empty[S] s_full[2] s_free[2] p_full[2][2] pv_done[2][2]
-    //           q_ready[2] fin[2] wg_bar[2]
+    //           q_ready[2] fin[2] turn[2]
     static constexpr int kNumBars = 2 * kStages + 18;
     static constexpr int kBarOffset = kPOffset + 4 * kPBytes;
     static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;  // tmem base, err, last[2]
@@ -422,7 +422,7 @@ struct Smem {
     __device__ uint32_t pv_done(int h, int b) const { return bars + 8 * (S2 + 8 + 2 * h + b); }
     __device__ uint32_t q_ready(int h) const { return bars + 8 * (S2 + 12 + h); }
     __device__ uint32_t fin(int h) const { return bars + 8 * (S2 + 14 + h); }
-    __device__ uint32_t wg_bar(int h) const { return bars + 8 * (S2 + 16 + h); }
+    __device__ uint32_t turn(int h) const { return bars + 8 * (S2 + 16 + h); }
     __device__ uint32_t p_tile(int h, int b) const { return pbuf + (2 * h + b) * Cfg<D>::kPBytes; }
 };
 
@@ -593,6 +593,10 @@ __device__ void role_softmax(const AttnArgs &a, Sched sch, const Smem<D> &sm, ui
     // O_h += P_h V of this half's tile number n has completed
     auto wait_pv = [&](uint32_t n) -> bool { return wait(sm.pv_done(h, n & 1), (n >> 1) & 1); };
     uint32_t spar = 0, cnt = 0;  // cnt: tiles of this half so far
+    // When both halves are active the two warpgroups take turns at the arithmetic of
+    // a tile (turn barriers): one computes while the other waits on its memory
+    // traffic and barriers, instead of both doing the same phase at once.
+    uint32_t tpar = h == 0 ? 1u : 0u;
     // this thread's P row inside a [128][64] bf16 tile, 128-byte swizzle
     const uint32_t prow = (r >> 3) * 1024 + (r & 7) * 128;
     bool ok = true;
@@ -645,10 +649,15 @@ __device__ void role_softmax(const AttnArgs &a, Sched sch, const Smem<D> &sm, ui
             // it by more than kRescaleLog2; otherwise P is taken against the stale max,
             // which leaves O / l unchanged (both carry the same factor) and lets the
             // exponentials start without waiting for this tile's max.
+            if (s.nh == 2) {
+                if (!wait(sm.turn(h), tpar)) { ok = false; break; }
+                tpar ^= 1;
+            }
             const float mx = tile_max(v);
             if (it == 0) m_run = mx * c;
             uint32_t pk[kTN / 2];
             float lsum = exp_tile(v, c, m_run, pk);
+            if (s.nh == 2) mbar_arrive(sm.turn(h ^ 1));
             if (it > 0) {
                 const float m_tile = mx * c;
                 const bool need = m_tile > m_run + kRescaleLog2;
@@ -818,6 +827,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_init(sm.pv_done(h, b), 1);
             }
             mbar_init(sm.q_ready(h), 128);
+            mbar_init(sm.turn(h), 128);
         }
         mbar_init(sm.fin(0), 1);
         mbar_init(sm.fin(1), 1);
