@@ -84,7 +84,8 @@ struct Cfg {
     static constexpr int kBarOffset = kPOffset + 4 * kPBytes;
     static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;  // tmem base, err, last[2]
     static constexpr int kPrefixOffset = kMiscOffset + 16;
-    static constexpr int smem_bytes(int npairs) { return 1024 + kPrefixOffset + (npairs + 1) * 4; }
+    // prefix: int[npairs + 1]; then tail: uint8[npairs] (keys in the last context tile)
+    static constexpr int smem_bytes(int npairs) { return 1024 + kPrefixOffset + (npairs + 1) * 4 + npairs; }
     static_assert(2 * kQCols + 2 * kTN + 2 * D <= kTmemCols, "TMEM budget");
 };
 
@@ -363,6 +364,7 @@ __device__ __forceinline__ int owner_of(int64_t t, int P, int64_t T) {
 
 struct Sched {
     const int *prefix;
+    const uint8_t *tail;  // keys in each pair's last context tile (0 when L_b = 0)
     int P;
     int64_t T, tcur, tend;
 
@@ -386,9 +388,9 @@ struct Sched {
             const int bg = p / a.NRG;
             s.g = bg % a.Hkv;
             s.b = bg / a.Hkv;
-            int L = a.lens[s.b];
-            s.L = L < 0 ? 0 : (L > a.Lmax ? a.Lmax : L);
-            s.nctx = (s.L + kTN - 1) / kTN;
+            // the context length comes from shared memory (no global read here)
+            s.nctx = static_cast<int>(pe - rs) - 1;
+            s.L = s.nctx == 0 ? 0 : (s.nctx - 1) * kTN + tail[p];
             s.rows = min(kRows, a.R - s.rg * kRows);
             s.nh = s.rows > 128 ? 2 : 1;
             s.tile0 = static_cast<int>(t0 - rs);
@@ -599,34 +601,42 @@ __device__ void role_softmax(const AttnArgs &a, Sched sch, const Smem<D> &sm, ui
     uint32_t tpar = h == 0 ? 1u : 0u;
     // this thread's P row inside a [128][64] bf16 tile, 128-byte swizzle
     const uint32_t prow = (r >> 3) * 1024 + (r & 7) * 128;
-    bool ok = true;
-    Seg s;
-    while (ok && sch.next(a, s)) {
-        if (h >= s.nh) continue;
-        const int rl = h * 128 + r;  // row within the pair
-        const bool valid = rl < s.rows;
-        {  // Q row -> TMEM (zeros for rows past the pair)
-            uint32_t qw[C::kQCols];
-            if (valid) {
-                const int rr = s.rg * kRows + rl;
-                const int sq = rr / a.G, head = s.g * a.G + rr % a.G;
-                const uint4 *src = reinterpret_cast<const uint4 *>(a.q + s.b * a.qs[0] +
-                                                                   sq * a.qs[1] + head * a.qs[2]);
+    const int rl = h * 128 + r;  // row within the pair
+    // Q row of segment q_seg -> TMEM (zeros for rows past the pair), then q_ready
+    auto load_q = [&](const Seg &q_seg) {
+        uint32_t qw[C::kQCols];
+        if (rl < q_seg.rows) {
+            const int rr = q_seg.rg * kRows + rl;
+            const int sq = rr / a.G, head = q_seg.g * a.G + rr % a.G;
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.q + q_seg.b * a.qs[0] +
+                                                               sq * a.qs[1] + head * a.qs[2]);
 #pragma unroll
-                for (int j = 0; j < D / 8; ++j) {
-                    const uint4 v = __ldg(src + j);
-                    qw[4 * j] = v.x; qw[4 * j + 1] = v.y; qw[4 * j + 2] = v.z; qw[4 * j + 3] = v.w;
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < C::kQCols; ++j) qw[j] = 0u;
+            for (int j = 0; j < D / 8; ++j) {
+                const uint4 v = __ldg(src + j);
+                qw[4 * j] = v.x; qw[4 * j + 1] = v.y; qw[4 * j + 2] = v.z; qw[4 * j + 3] = v.w;
             }
+        } else {
 #pragma unroll
-            for (int j = 0; j < C::kQCols / 32; ++j) tmem_st32(tl + C::colQ(h) + 32 * j, qw + 32 * j);
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(sm.q_ready(h));
+            for (int j = 0; j < C::kQCols; ++j) qw[j] = 0u;
         }
+#pragma unroll
+        for (int j = 0; j < C::kQCols / 32; ++j) tmem_st32(tl + C::colQ(h) + 32 * j, qw + 32 * j);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(sm.q_ready(h));
+    };
+    // next segment in which this half takes part
+    auto next_mine = [&](Seg &n) -> bool {
+        while (sch.next(a, n))
+            if (h < n.nh) return true;
+        return false;
+    };
+    bool ok = true;
+    Seg s, nxt;
+    bool have = next_mine(s);
+    if (have) load_q(s);
+    while (ok && have) {
+        const bool valid = rl < s.rows;
         float m_run = -INFINITY, l_run = 0.f;
         for (int it = 0; it < s.ntiles; ++it) {
             const int nvalid = tile_valid(a, s, s.tile0 + it);
@@ -697,6 +707,11 @@ __device__ void role_softmax(const AttnArgs &a, Sched sch, const Smem<D> &sm, ui
             ++cnt;
         }
         if (!ok) break;
+        // The next segment's Q goes into TMEM before this segment's epilogue (the last
+        // Q K^T of this segment has completed: its S was read), so the MMA warp can
+        // start on the next segment while O is read out and stored.
+        const bool have_next = next_mine(nxt);
+        if (have_next) load_q(nxt);
         // ---- segment epilogue: O_h is final once the last P_h V is done
         if (!wait_pv(cnt - 1)) { ok = false; break; }
         tc_fence_after();
@@ -715,24 +730,26 @@ __device__ void role_softmax(const AttnArgs &a, Sched sch, const Smem<D> &sm, ui
                 }
             }
             if (valid) store_lse(a, s, rl, m_run, l_run);
-            continue;
-        }
-        // ---- split pair: write this CTA's partial (O / l, m, l); block_attn_merge_kernel
-        // combines the partials once the whole grid has finished
-        const size_t slot = static_cast<size_t>(blockIdx.x + s.p);
-        const float inv = 1.f / l_run;
+        } else {
+            // ---- split pair: write this CTA's partial (O / l, m, l); block_attn_merge_kernel
+            // combines the partials once the whole grid has finished
+            const size_t slot = static_cast<size_t>(blockIdx.x + s.p);
+            const float inv = 1.f / l_run;
 #pragma unroll 1
-        for (int j = 0; j < D / 32; ++j) {
-            uint32_t o[32];
-            tmem_ld32(tl + C::colO(h) + 32 * j, o);
-            tmem_wait_ld(o);
-            if (valid) {
-                float *dst = a.part_o + (slot * D + 32 * j) * kRows + rl;
+            for (int j = 0; j < D / 32; ++j) {
+                uint32_t o[32];
+                tmem_ld32(tl + C::colO(h) + 32 * j, o);
+                tmem_wait_ld(o);
+                if (valid) {
+                    float *dst = a.part_o + (slot * D + 32 * j) * kRows + rl;
 #pragma unroll
-                for (int e = 0; e < 32; ++e) __stcg(dst + e * kRows, __uint_as_float(o[e]) * inv);
+                    for (int e = 0; e < 32; ++e) __stcg(dst + e * kRows, __uint_as_float(o[e]) * inv);
+                }
             }
+            if (valid) __stcg(a.part_ml + slot * kRows + rl, make_float2(m_run, l_run));
         }
-        if (valid) __stcg(a.part_ml + slot * kRows + rl, make_float2(m_run, l_run));
+        s = nxt;
+        have = have_next;
     }
 }
 
@@ -748,6 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t raw = smem_u32(smem_raw);
     unsigned char *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // 1024-byte aligned
     int *prefix = reinterpret_cast<int *>(smem + C::kPrefixOffset);
+    uint8_t *tail = reinterpret_cast<uint8_t *>(prefix + a.npairs + 1);
     int *misc = reinterpret_cast<int *>(smem + C::kMiscOffset);
     __shared__ int warp_sums[kThreads / 32];
 
@@ -787,7 +805,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefix[p] = run;
             int L = a.lens[p / (a.Hkv * a.NRG)];
             L = L < 0 ? 0 : (L > a.Lmax ? a.Lmax : L);
-            run += (L + kTN - 1) / kTN + 1 + kSegCost;
+            const int nctx = (L + kTN - 1) / kTN;
+            tail[p] = static_cast<uint8_t>(nctx == 0 ? 0 : L - (nctx - 1) * kTN);
+            run += nctx + 1 + kSegCost;
         }
         if (t == kThreads - 1) prefix[a.npairs] = run;
         __syncthreads();
@@ -848,6 +868,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     Sched sch;
     sch.prefix = prefix;
+    sch.tail = tail;
     sch.P = P;
     sch.T = T;
     sch.tcur = static_cast<int64_t>(cta) * T / P;
@@ -877,15 +898,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 //   lse = (M + log2 sum_c 2^(m_c-M) l_c) ln 2.
 // Block = (pair, 32-row chunk of the pair's 256 rows), 8 warps; warp w owns d/8
 // columns and lane i row i of the chunk, so every load of a partial is a coalesced
-// 128-byte line, and the loads of up to 8 partials are issued before any is used.
+// 128-byte line; partials are folded in one at a time with a running maximum.
 // Launched as a programmatic dependent of the attention kernel: griddepcontrol.wait
 // returns once that grid has completed and its writes are visible.
 constexpr int kMergeThreads = 256;
 template <int D>
-__global__ void __launch_bounds__(kMergeThreads) block_attn_merge_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(kMergeThreads, 4) block_attn_merge_kernel(const AttnArgs a) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     constexpr int kCols = D / 8;
-    constexpr int kBatch = 8;
     const int p = blockIdx.x >> 3, chunk = blockIdx.x & 7;
     const int2 cs = a.pair_split[p];
     if (cs.x == cs.y) return;  // finished inside one CTA
@@ -895,43 +915,24 @@ __global__ void __launch_bounds__(kMergeThreads) block_attn_merge_kernel(const A
     const int rl = chunk * 32 + lane;
     if (rl >= rows) return;
     const float2 *mlp = a.part_ml + static_cast<size_t>(p) * kRows + rl;  // + c * kRows
+    const float *op = a.part_o + (static_cast<size_t>(p) * D + kCols * warp) * kRows + rl;
     float M = -INFINITY, den = 0.f;
     float acc[kCols];
 #pragma unroll
     for (int e = 0; e < kCols; ++e) acc[e] = 0.f;
-    for (int c0 = cs.x; c0 <= cs.y; c0 += kBatch) {
-        float2 ml[kBatch];
-        float v[kBatch][kCols];
+#pragma unroll 2
+    for (int c = cs.x; c <= cs.y; ++c) {
+        const float2 ml = __ldcg(mlp + static_cast<size_t>(c) * kRows);
+        const float *src = op + static_cast<size_t>(c) * D * kRows;
+        float v[kCols];
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const int c = c0 + u;
-            if (c <= cs.y) {
-                ml[u] = __ldcg(mlp + static_cast<size_t>(c) * kRows);
-                const float *src =
-                    a.part_o + (static_cast<size_t>(c + p) * D + kCols * warp) * kRows + rl;
+        for (int e = 0; e < kCols; ++e) v[e] = __ldcg(src + e * kRows);
+        const float Mn = fmaxf(M, ml.x);
+        const float so = ex2_approx(M - Mn), w = ex2_approx(ml.x - Mn) * ml.y;
+        M = Mn;
+        den = den * so + w;
 #pragma unroll
-                for (int e = 0; e < kCols; ++e) v[u][e] = __ldcg(src + e * kRows);
-            } else {
-                ml[u] = make_float2(-INFINITY, 0.f);
-#pragma unroll
-                for (int e = 0; e < kCols; ++e) v[u][e] = 0.f;
-            }
-        }
-        float Mb = M;
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) Mb = fmaxf(Mb, ml[u].x);
-        const float so = ex2_approx(M - Mb);
-        den *= so;
-#pragma unroll
-        for (int e = 0; e < kCols; ++e) acc[e] *= so;
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            const float w = ex2_approx(ml[u].x - Mb) * ml[u].y;
-            den += w;
-#pragma unroll
-            for (int e = 0; e < kCols; ++e) acc[e] += w * v[u][e];
-        }
-        M = Mb;
+        for (int e = 0; e < kCols; ++e) acc[e] = acc[e] * so + w * v[e];
     }
     const float inv = 1.f / den;
     const int rr = rg * kRows + rl;
