@@ -54,7 +54,7 @@ constexpr int kMaxPairs = 4096;
 constexpr int kMinTiles = 4;  // smallest tile range worth a partial
 // Cost of starting a segment (Q load, pipeline refill, epilogue), in tile units: every
 // pair is charged this many extra units at its start when the tile ranges are cut.
-constexpr int kSegCost = 3;
+constexpr int kSegCost = 5;
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kRescaleLog2 = 8.f;  // lazy rescale: O is rescaled when the max grows by > 2^8
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
