@@ -56,4 +56,112 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
+// ---------------------------------------------------------------- mbarriers
+// Every wait on an mbarrier is bounded: after kWaitLimitNs it records an error code
+// and returns false, so a kernel that would otherwise wait forever stops instead.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+// Waits for the phase of `parity` to complete.  Gives up (false) when another
+// role has flagged an error or after kWaitLimitNs, flagging `code`.  Thread-level
+// (the TMA producer runs on one thread).
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *err,
+                                            int code) {
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try(bar, parity)) return true;
+        if ((i & 63) == 0) {
+            if (*err) return false;
+            if (globaltimer() - t0 > kWaitLimitNs) {
+                atomicCAS(const_cast<int *>(err), 0, code);
+                return false;
+            }
+        }
+    }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *err,
+                                          int code) {
+    if (mbar_try(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, err, code);
+}
+// Warp-collective form: every lane of a converged warp calls it and all get the
+// same answer.  Inline, so a wait that is already satisfied costs a few cycles.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *err,
+                                          int code) {
+    if (__any_sync(0xFFFFFFFFu, mbar_try(bar, parity))) return true;
+    uint64_t t0 = 0;
+    for (uint32_t i = 1;; ++i) {
+        if (__any_sync(0xFFFFFFFFu, mbar_try(bar, parity))) return true;
+        if ((i & 255) == 0) {
+            int stop = 0;
+            if ((threadIdx.x & 31) == 0) {
+                const uint64_t now = globaltimer();
+                if (t0 == 0) t0 = now;
+                if (*err) {
+                    stop = 1;
+                } else if (now - t0 > kWaitLimitNs) {
+                    atomicCAS(const_cast<int *>(err), 0, code);
+                    stop = 1;
+                }
+            }
+            if (__shfl_sync(0xFFFFFFFFu, stop, 0)) return false;
+        }
+    }
+}
+// Bounded wait that ignores the error flag (used to drain copies in flight).
+static __device__ __noinline__ bool mbar_drain(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try(bar, parity))
+        if (globaltimer() - t0 > kWaitLimitNs) return false;
+    return true;
+}
+
+// TMA tile load; `policy` is an L2 cache policy (createpolicy).
+
+// Bulk copy global -> shared (16-byte aligned, size a multiple of 16) completing
+// on an mbarrier; `policy` is an L2 cache policy (createpolicy).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                          uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+// Data read once: first in line for eviction from L2.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 }  // namespace tt
