@@ -37,6 +37,7 @@
 // the workspace and lets the CTA drain its copies and free TMEM.
 #include <cuda.h>
 #include <math.h>
+#include <string.h>
 
 #include <mutex>
 
@@ -339,7 +340,7 @@ __device__ void role_producer(const AttnArgs &a, Sched sch, const Smem<D> &sm,
                               const CUtensorMap *tkc, const CUtensorMap *tvc,
                               const CUtensorMap *tkb, const CUtensorMap *tvb) {
     using C = Cfg<D>;
-    int stage = 0;
+    int stage = 0, nissued = 0;
     uint32_t phase = 0, issued = 0, last_par = 0;
     // K/V tiles are read once: first in line for eviction from L2, so they do not
     // push out the partials the merge reads back
@@ -367,6 +368,10 @@ __device__ void role_producer(const AttnArgs &a, Sched sch, const Smem<D> &sm,
             issued |= 1u << stage;
             last_par = (last_par & ~(1u << stage)) | (phase << stage);
             if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+            // At kernel start every SM asks for its first K/V tiles at once; the first
+            // segment's Q (loaded by the softmax warps) would queue behind them.  After
+            // one tile, wait for that Q before filling the rest of the ring.
+            if (ok && ++nissued == 1 && !mbar_wait(sm.q_ready(0), 0, sm.err, 1)) ok = false;
         }
     }
     // no copy may still be landing when the CTA exits
@@ -575,7 +580,7 @@ __device__ void role_softmax(const AttnArgs &a, Sched sch, const Smem<D> &sm, ui
             if (it == 0) m_run = mx * c;
             uint32_t pk[kTN / 2];
             float lsum = exp_tile(v, c, m_run, pk);
-            if (s.nh == 2) mbar_arrive(sm.turn(h ^ 1));
+            if (s.nh == 2) mbar_arrive_after(sm.turn(h ^ 1), lsum);
             if (it > 0) {
                 const float m_tile = mx * c;
                 const bool need = m_tile > m_run + kRescaleLog2;
@@ -959,29 +964,73 @@ tt_status make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, u
     return TT_OK;
 }
 
-template <int D>
-tt_status launch(const tt_attn_desc *d, const AttnArgs &a, const void *k_ctx, const void *v_ctx,
-                 const void *k_blk, const void *v_blk, cudaStream_t stream, const char *fn) {
+// The four tensor maps of a call depend only on pointers, shape and strides; a small
+// per-thread cache skips re-encoding them for repeated calls on the same buffers
+// (a decode loop calls every layer with the same caches step after step).
+struct MapKey {
+    const void *k_ctx, *v_ctx, *k_blk, *v_blk;
+    int32_t B, S, Hkv, Lmax, d;
+    int64_t kc[4], vc[4], kb[4], vb[4];
+    bool operator==(const MapKey &o) const { return memcmp(this, &o, sizeof(MapKey)) == 0; }
+};
+struct MapEntry {
+    MapKey key;
     CUtensorMap kc, vc, kb, vb;
+    bool used;
+};
+constexpr int kMapCache = 16;
+
+template <int D>
+tt_status encode_maps(const tt_attn_desc *d, const void *k_ctx, const void *v_ctx, const void *k_blk,
+                      const void *v_blk, MapEntry *e, const char *fn) {
     tt_status st;
     const uint64_t B = d->B, S = d->S, Hkv = d->Hkv, Lmax = d->Lmax;
-    if ((st = make_map(&kb, k_blk, D, Hkv, S, B, d->kblk_strides[2], d->kblk_strides[1],
+    if ((st = make_map(&e->kb, k_blk, D, Hkv, S, B, d->kblk_strides[2], d->kblk_strides[1],
                        d->kblk_strides[0], 1, 64, fn, "k_blk")) != TT_OK)
         return st;
-    if ((st = make_map(&vb, v_blk, D, Hkv, S, B, d->vblk_strides[2], d->vblk_strides[1],
+    if ((st = make_map(&e->vb, v_blk, D, Hkv, S, B, d->vblk_strides[2], d->vblk_strides[1],
                        d->vblk_strides[0], 1, 64, fn, "v_blk")) != TT_OK)
         return st;
     if (Lmax > 0) {
-        if ((st = make_map(&kc, k_ctx, D, Lmax, Hkv, B, d->kctx_strides[2], d->kctx_strides[1],
+        if ((st = make_map(&e->kc, k_ctx, D, Lmax, Hkv, B, d->kctx_strides[2], d->kctx_strides[1],
                            d->kctx_strides[0], 64, 1, fn, "k_ctx")) != TT_OK)
             return st;
-        if ((st = make_map(&vc, v_ctx, D, Lmax, Hkv, B, d->vctx_strides[2], d->vctx_strides[1],
+        if ((st = make_map(&e->vc, v_ctx, D, Lmax, Hkv, B, d->vctx_strides[2], d->vctx_strides[1],
                            d->vctx_strides[0], 64, 1, fn, "v_ctx")) != TT_OK)
             return st;
     } else {  // no context rows: the context maps are never used
-        kc = kb;
-        vc = vb;
+        e->kc = e->kb;
+        e->vc = e->vb;
     }
+    return TT_OK;
+}
+
+
+template <int D>
+tt_status launch(const tt_attn_desc *d, const AttnArgs &a, const void *k_ctx, const void *v_ctx,
+                 const void *k_blk, const void *v_blk, cudaStream_t stream, const char *fn) {
+    thread_local MapEntry cache[kMapCache] = {};
+    thread_local int next_slot = 0;
+    MapKey key;
+    memset(&key, 0, sizeof key);
+    key.k_ctx = k_ctx; key.v_ctx = v_ctx; key.k_blk = k_blk; key.v_blk = v_blk;
+    key.B = d->B; key.S = d->S; key.Hkv = d->Hkv; key.Lmax = d->Lmax; key.d = d->d;
+    memcpy(key.kc, d->kctx_strides, sizeof key.kc);
+    memcpy(key.vc, d->vctx_strides, sizeof key.vc);
+    memcpy(key.kb, d->kblk_strides, sizeof key.kb);
+    memcpy(key.vb, d->vblk_strides, sizeof key.vb);
+    MapEntry *hit = nullptr;
+    for (int i = 0; i < kMapCache && !hit; ++i)
+        if (cache[i].used && cache[i].key == key) hit = &cache[i];
+    if (!hit) {
+        tt_status st = encode_maps<D>(d, k_ctx, v_ctx, k_blk, v_blk, &cache[next_slot], fn);
+        if (st != TT_OK) return st;
+        cache[next_slot].key = key;
+        cache[next_slot].used = true;
+        hit = &cache[next_slot];
+        next_slot = (next_slot + 1) % kMapCache;
+    }
+    const CUtensorMap &kc = hit->kc, &vc = hit->vc, &kb = hit->kb, &vb = hit->vb;
     static std::mutex mu;
     static bool configured[64] = {false};
     int dev = 0;

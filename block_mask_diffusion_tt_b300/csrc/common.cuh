@@ -86,6 +86,14 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// Arrive that takes `after` as an input, so the arithmetic producing it cannot be
+// scheduled below the arrive (a volatile asm orders memory accesses, not arithmetic).
+__device__ __forceinline__ void mbar_arrive_after(uint32_t bar, float after) {
+    asm volatile("{\n\t.reg .f32 dep;\n\tmov.f32 dep, %1;\n\t"
+                 "mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}\n" ::"r"(bar),
+                 "f"(after)
+                 : "memory");
+}
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
