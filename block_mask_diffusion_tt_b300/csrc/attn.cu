@@ -21,18 +21,24 @@
 //    launched as a programmatic dependent, merges them: M = max m_c,
 //    O = sum 2^(m_c-M) l_c O_c / sum 2^(m_c-M) l_c.  No CTA waits on another.
 //
-// Inside a CTA (320 threads, one CTA per SM, 512 TMEM columns):
+// Inside a CTA (352 threads, one CTA per SM, 512 TMEM columns):
 //  warp 8     TMA producer: K and V tiles (64 keys x d, 128-byte swizzle) into a
 //             ring of shared-memory stages (full/empty mbarriers);
-//  warp 9     MMA issuer: S_h = Q_h K^T (A = Q_h in TMEM, B = K tile in smem,
-//             M=128 N=64), then O_h += P_h V (A = P_h in TMEM, B = V tile read
-//             MN-major, M=128 N=d); completion via tcgen05.commit;
+//  warps 9,10 MMA issuers, one per half: S_h = Q_h K^T (A = Q_h in shared memory,
+//             B = K tile, M=128 N=64) into one of two S buffers of the half, then
+//             O_h += P_h V (A = P_h in TMEM, B = V tile read MN-major, M=128 N=d);
+//             completion via tcgen05.commit;
 //  warps 0-7  softmax, warpgroup h owns half h, one query row per thread: reads
 //             its S row from TMEM, keeps the running max (in log2 units, raised
 //             only when it grows by more than 8, so O is rescaled rarely) and
-//             sum, writes P = 2^(x - m) as bf16 over the S columns, and at the
-//             end of a segment reads O, normalises and stores it.
-// TMEM columns (d=128): Q_0 Q_1 [64 each] | S_0 S_1 [64 each] | O_0 O_1 [128 each].
+//             sum, writes P = 2^(x - m) as bf16 pairs over the first 32 columns of
+//             the same S buffer, and at the end of a segment reads O, normalises
+//             and stores it.
+// With two S buffers per half the MMA warp computes the scores of tile j+1 while
+// the softmax works on tile j.  An S buffer is rewritten by Q K^T of tile j+2 only
+// after P V of tile j, which reads the P stored there, has been issued by the same
+// warp; tcgen05 operations of one thread run in issue order.
+// TMEM columns (d=128): O_0 O_1 [128 each] | S/P_0 [2 x 64] | S/P_1 [2 x 64].
 // Every wait on an mbarrier gives up after 2 s (globaltimer), records a flag in
 // the workspace and lets the CTA drain its copies and free TMEM.
 #include <cuda.h>
@@ -66,27 +72,26 @@ struct Cfg {
     static constexpr int kRegionBytes = kTN * 128;    // one chunk of a 64-key tile
     static constexpr int kStageBytes = 2 * kChunks * kRegionBytes;  // K chunks then V chunks
     static constexpr int kStages = D == 128 ? 4 : 6;
-    static constexpr int kPBytes = 128 * kTN * 2;     // P of one half, bf16 [128 rows][64 keys]
-    static constexpr int kPOffset = kStages * kStageBytes;  // P[half][buffer]
-    static constexpr int kQCols = D / 2;  // bf16 pairs per row
-    __host__ __device__ static constexpr uint32_t colQ(int h) { return h * kQCols; }
-    __host__ __device__ static constexpr uint32_t colS(int h) { return 2 * kQCols + h * kTN; }
-    __host__ __device__ static constexpr uint32_t colO(int h) { return 2 * kQCols + 2 * kTN + h * D; }
-    // instruction descriptors (kind::f16): D fp32, A/B bf16, M=128.  S = Q K^T: A in
-    // TMEM, B = K tile K-major, N=64.  O += P V: A = P K-major, B = V MN-major, N=d.
+    static constexpr int kQRegion = 128 * 128;  // one 64-column chunk of a half's 128 Q rows
+    static constexpr int kQHalfBytes = kChunks * kQRegion;
+    static constexpr int kQOffset = kStages * kStageBytes;  // Q[half][chunk][128 rows][128 B]
+    __host__ __device__ static constexpr uint32_t colO(int h) { return h * D; }
+    __host__ __device__ static constexpr uint32_t colS(int h, int b) { return 2 * D + (2 * h + b) * kTN; }
+    // instruction descriptors (kind::f16): D fp32, A/B bf16, M=128.  S = Q K^T: A = Q
+    // and B = K tile, both K-major, N=64.  O += P V: A = P (TMEM), B = V MN-major, N=d.
     static constexpr uint32_t kIdescQK = (1u << 4) | (1u << 7) | (1u << 10) |
                                          (uint32_t(kTN >> 3) << 17) | (uint32_t(128 >> 4) << 24);
     static constexpr uint32_t kIdescPV = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
                                          (uint32_t(D >> 3) << 17) | (uint32_t(128 >> 4) << 24);
-    // barriers: full[S] empty[S] s_full[2] s_free[2] p_full[2][2] pv_done[2][2]
+    // barriers: full[S] empty[S] s_full[2][2] p_full[2][2] pv_done[2][2]
     //           q_ready[2] fin[2] turn[2]
     static constexpr int kNumBars = 2 * kStages + 18;
-    static constexpr int kBarOffset = kPOffset + 4 * kPBytes;
+    static constexpr int kBarOffset = kQOffset + 2 * kQHalfBytes;
     static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;  // tmem base, err, last[2]
     static constexpr int kPrefixOffset = kMiscOffset + 16;
     // prefix: int[npairs + 1]; then tail: uint8[npairs] (keys in the last context tile)
     static constexpr int smem_bytes(int npairs) { return 1024 + kPrefixOffset + (npairs + 1) * 4 + npairs; }
-    static_assert(2 * kQCols + 2 * kTN + 2 * D <= kTmemCols, "TMEM budget");
+    static_assert(2 * D + 4 * kTN <= kTmemCols, "TMEM budget");
 };
 
 struct AttnArgs {
@@ -317,7 +322,7 @@ __device__ __forceinline__ int tile_valid(const AttnArgs &a, const Seg &s, int t
 // ---------------------------------------------------------------- roles
 template <int D>
 struct Smem {
-    uint32_t stages, pbuf, bars;
+    uint32_t stages, qbuf, bars;
     int *prefix;
     volatile int *err;
     volatile int *last;
@@ -325,14 +330,13 @@ struct Smem {
     static constexpr int S2 = 2 * Cfg<D>::kStages;
     __device__ uint32_t full(int i) const { return bars + 8 * i; }
     __device__ uint32_t empty(int i) const { return bars + 8 * (Cfg<D>::kStages + i); }
-    __device__ uint32_t s_full(int h) const { return bars + 8 * (S2 + h); }
-    __device__ uint32_t s_free(int h) const { return bars + 8 * (S2 + 2 + h); }
+    __device__ uint32_t s_full(int h, int b) const { return bars + 8 * (S2 + 2 * h + b); }
     __device__ uint32_t p_full(int h, int b) const { return bars + 8 * (S2 + 4 + 2 * h + b); }
     __device__ uint32_t pv_done(int h, int b) const { return bars + 8 * (S2 + 8 + 2 * h + b); }
     __device__ uint32_t q_ready(int h) const { return bars + 8 * (S2 + 12 + h); }
     __device__ uint32_t fin(int h) const { return bars + 8 * (S2 + 14 + h); }
     __device__ uint32_t turn(int h) const { return bars + 8 * (S2 + 16 + h); }
-    __device__ uint32_t p_tile(int h, int b) const { return pbuf + (2 * h + b) * Cfg<D>::kPBytes; }
+    __device__ uint32_t q_tile(int h) const { return qbuf + h * Cfg<D>::kQHalfBytes; }
 };
 
 template <int D>
@@ -379,12 +383,13 @@ __device__ void role_producer(const AttnArgs &a, Sched sch, const Smem<D> &sm,
         if (issued >> st & 1u) mbar_drain(sm.full(st), last_par >> st & 1u);
 }
 
-// MMA warp of half h (warp 9 + h).  It runs one tile ahead on Q K^T: at step it it
-// issues S_h = Q_h K^T for tile it (once the softmax has read S_h of tile it-1)
-// and then O_h += P_h V for tile it-1 (once its P is in shared memory), so the
-// tensor core computes the next scores while the softmax warps work on the current
-// ones.  The two halves run independently; a K/V stage is released when both MMA
-// warps have finished with it (empty barrier of count 2).
+// MMA warp of half h (warp 9 + h).  At step it it issues S_h = Q_h K^T for tile it
+// into S buffer it&1 and then O_h += P_h V for tile it-1 (once the softmax has
+// written that P over its S buffer).  Buffer it&1 last held tile it-2, whose P V
+// this warp issued one step earlier, so the scores of the next tile are computed
+// while the softmax works on the current one.  The two halves run independently; a
+// K/V stage is released when both MMA warps have finished with it (empty barrier
+// of count 2).
 template <int D>
 __device__ void role_mma(const AttnArgs &a, Sched sch, const Smem<D> &sm, uint32_t tmem, int h) {
     using C = Cfg<D>;
@@ -394,8 +399,8 @@ __device__ void role_mma(const AttnArgs &a, Sched sch, const Smem<D> &sm, uint32
     const uint64_t kdesc0 = sdesc_sw128(sm.stages, 16, 1024);
     const uint64_t vdesc0 =
         sdesc_sw128(sm.stages + C::kChunks * C::kRegionBytes, C::kRegionBytes, 1024);
-    const uint64_t pdesc0 = sdesc_sw128(sm.pbuf, 16, 1024) + (((2 * h) * C::kPBytes) >> 4);
-    const uint32_t d_s = tmem + C::colS(h), d_o = tmem + C::colO(h), a_q = tmem + C::colQ(h);
+    const uint64_t qdesc0 = sdesc_sw128(sm.q_tile(h), 16, 1024);
+    const uint32_t d_o = tmem + C::colO(h);
     int stage = 0, prev_stage = 0;
     uint32_t phase = 0, qpar = 0, s_cnt = 0, p_cnt = 0;
     bool ok = true;
@@ -434,16 +439,16 @@ __device__ void role_mma(const AttnArgs &a, Sched sch, const Smem<D> &sm, uint32
                     if (!wait(sm.q_ready(h), qpar)) { ok = false; break; }
                     qpar ^= 1;
                 }
-                // S_h is free once the softmax has read the previous one
-                if (s_cnt > 0 && !wait(sm.s_free(h), (s_cnt - 1) & 1)) { ok = false; break; }
                 tc_fence_after();
+                const uint32_t d_s = tmem + C::colS(h, s_cnt & 1);
                 const uint64_t kd = kdesc0 + ((stage * C::kStageBytes) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    tc_mma_ts_e(d_s, a_q + kk * 8,
-                                kd + (((kk >> 2) * C::kRegionBytes + (kk & 3) * 32) >> 4),
-                                C::kIdescQK, kk > 0);
-                tc_commit_e(sm.s_full(h));
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t koff = (kk >> 2) * C::kRegionBytes + (kk & 3) * 32;
+                    const uint32_t qoff = (kk >> 2) * C::kQRegion + (kk & 3) * 32;
+                    tc_mma_ss_e(d_s, qdesc0 + (qoff >> 4), kd + (koff >> 4), C::kIdescQK, kk > 0);
+                }
+                tc_commit_e(sm.s_full(h, s_cnt & 1));
                 ++s_cnt;
             }
             if (it > 0) {  // O_h += P_h V for the previous tile
@@ -451,10 +456,10 @@ __device__ void role_mma(const AttnArgs &a, Sched sch, const Smem<D> &sm, uint32
                 if (!wait(sm.p_full(h, b), (p_cnt >> 1) & 1)) { ok = false; break; }
                 tc_fence_after();
                 const uint64_t vd = vdesc0 + ((prev_stage * C::kStageBytes) >> 4);
-                const uint64_t pd = pdesc0 + ((b * C::kPBytes) >> 4);
+                const uint32_t a_p = tmem + C::colS(h, b);  // P: 16 keys per 8 columns
 #pragma unroll
                 for (int kk = 0; kk < kTN / 16; ++kk)
-                    tc_mma_ss_e(d_o, pd + ((kk * 32) >> 4), vd + ((kk * 2048) >> 4), C::kIdescPV,
+                    tc_mma_ts_e(d_o, a_p + kk * 8, vd + ((kk * 2048) >> 4), C::kIdescPV,
                                 (it > 1 || kk > 0) ? 1u : 0u);
                 tc_commit_e(sm.pv_done(h, b));
                 ++p_cnt;
@@ -507,35 +512,37 @@ __device__ void role_softmax(const AttnArgs &a, Sched sch, const Smem<D> &sm, ui
     auto wait = [&](uint32_t bar, uint32_t par) -> bool { return warp_wait(bar, par, sm.err, 3); };
     // O_h += P_h V of this half's tile number n has completed
     auto wait_pv = [&](uint32_t n) -> bool { return wait(sm.pv_done(h, n & 1), (n >> 1) & 1); };
-    uint32_t spar = 0, cnt = 0;  // cnt: tiles of this half so far
+    uint32_t cnt = 0;  // tiles of this half so far; tile n uses S buffer n & 1
     // When both halves are active the two warpgroups take turns at the arithmetic of
     // a tile (turn barriers): one computes while the other waits on its memory
     // traffic and barriers, instead of both doing the same phase at once.
     uint32_t tpar = h == 0 ? 1u : 0u;
-    // this thread's P row inside a [128][64] bf16 tile, 128-byte swizzle
-    const uint32_t prow = (r >> 3) * 1024 + (r & 7) * 128;
     const int rl = h * 128 + r;  // row within the pair
-    // Q row of segment q_seg -> TMEM (zeros for rows past the pair), then q_ready
+    // this thread's Q row inside a [128 rows][128 B] chunk, 128-byte swizzle
+    const uint32_t qrow = sm.q_tile(h) + (r >> 3) * 1024 + (r & 7) * 128;
+    // Q row of segment q_seg -> shared memory, K-major in 64-column chunks with the
+    // 128-byte swizzle of the K tiles (zeros for rows past the pair), then q_ready.
+    // The caller makes sure no Q K^T still reads the previous Q.
     auto load_q = [&](const Seg &q_seg) {
-        uint32_t qw[C::kQCols];
+        uint4 qv[D / 8];
         if (rl < q_seg.rows) {
             const int rr = q_seg.rg * kRows + rl;
             const int sq = rr / a.G, head = q_seg.g * a.G + rr % a.G;
             const uint4 *src = reinterpret_cast<const uint4 *>(a.q + q_seg.b * a.qs[0] +
                                                                sq * a.qs[1] + head * a.qs[2]);
 #pragma unroll
-            for (int j = 0; j < D / 8; ++j) {
-                const uint4 v = __ldg(src + j);
-                qw[4 * j] = v.x; qw[4 * j + 1] = v.y; qw[4 * j + 2] = v.z; qw[4 * j + 3] = v.w;
-            }
+            for (int j = 0; j < D / 8; ++j) qv[j] = __ldg(src + j);
         } else {
 #pragma unroll
-            for (int j = 0; j < C::kQCols; ++j) qw[j] = 0u;
+            for (int j = 0; j < D / 8; ++j) qv[j] = make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
-        for (int j = 0; j < C::kQCols / 32; ++j) tmem_st32(tl + C::colQ(h) + 32 * j, qw + 32 * j);
-        tmem_wait_st();
-        tc_fence_before();
+        for (int j = 0; j < D / 8; ++j)
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             qrow + (j >> 3) * C::kQRegion + (((j & 7) ^ (r & 7)) << 4)),
+                         "r"(qv[j].x), "r"(qv[j].y), "r"(qv[j].z), "r"(qv[j].w)
+                         : "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         mbar_arrive(sm.q_ready(h));
     };
     // next segment in which this half takes part
@@ -553,16 +560,14 @@ __device__ void role_softmax(const AttnArgs &a, Sched sch, const Smem<D> &sm, ui
         float m_run = -INFINITY, l_run = 0.f;
         for (int it = 0; it < s.ntiles; ++it) {
             const int nvalid = tile_valid(a, s, s.tile0 + it);
-            if (!wait(sm.s_full(h), spar)) { ok = false; break; }
-            spar ^= 1;
+            const uint32_t sb = C::colS(h, cnt & 1);
+            if (!wait(sm.s_full(h, cnt & 1), (cnt >> 1) & 1)) { ok = false; break; }
             tc_fence_after();
             uint32_t v[kTN];
-            tmem_ld32(tl + C::colS(h), v);
-            tmem_ld32(tl + C::colS(h) + 32, v + 32);
+            tmem_ld32(tl + sb, v);
+            tmem_ld32(tl + sb + 32, v + 32);
             tmem_wait_ld(v);
             tmem_touch(v + 32);
-            tc_fence_before();
-            mbar_arrive(sm.s_free(h));  // the MMA warp may overwrite S_h now
             if (nvalid < kTN) {
 #pragma unroll
                 for (int j = 0; j < kTN; ++j)
@@ -604,17 +609,9 @@ __device__ void role_softmax(const AttnArgs &a, Sched sch, const Smem<D> &sm, ui
                 }
             }
             l_run += lsum;
-            // the P buffer of this tile was last read by the P V two tiles back
-            if (cnt >= 2 && !wait_pv(cnt - 2)) { ok = false; break; }
-            const uint32_t pt = sm.p_tile(h, cnt & 1) + prow;
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
-                                 pt + ((ch ^ (r & 7)) << 4)),
-                             "r"(pk[4 * ch]), "r"(pk[4 * ch + 1]), "r"(pk[4 * ch + 2]),
-                             "r"(pk[4 * ch + 3])
-                             : "memory");
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            // P (bf16 pairs) over the first 32 columns of this tile's S buffer
+            tmem_st32(tl + sb, pk);
+            tmem_wait_st();
             tc_fence_before();
             mbar_arrive(sm.p_full(h, cnt & 1));
             ++cnt;
@@ -741,7 +738,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     Smem<D> sm;
     sm.stages = smem_u32(smem);
-    sm.pbuf = smem_u32(smem + C::kPOffset);
+    sm.qbuf = smem_u32(smem + C::kQOffset);
     sm.bars = smem_u32(smem + C::kBarOffset);
     sm.prefix = prefix;
     sm.tmem_slot = reinterpret_cast<uint32_t *>(misc);
@@ -753,9 +750,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(sm.empty(i), 2);
         }
         for (int h = 0; h < 2; ++h) {
-            mbar_init(sm.s_full(h), 1);
-            mbar_init(sm.s_free(h), 128);
             for (int b = 0; b < 2; ++b) {
+                mbar_init(sm.s_full(h, b), 1);
                 mbar_init(sm.p_full(h, b), 128);
                 mbar_init(sm.pv_done(h, b), 1);
             }
