@@ -805,17 +805,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Combines the partials of every pair whose tiles were split across CTAs:
 //   M = max_c m_c,  out = sum_c 2^(m_c-M) l_c (O_c/l_c) / sum_c 2^(m_c-M) l_c,
 //   lse = (M + log2 sum_c 2^(m_c-M) l_c) ln 2.
-// Block = (pair, 32-row chunk of the pair's 256 rows), 8 warps; warp w owns d/8
-// columns and lane i row i of the chunk, so every load of a partial is a coalesced
-// 128-byte line; partials are folded in one at a time with a running maximum.
+// Block = (pair, 32-row chunk of the pair's 256 rows, 64-column chunk), 8 warps;
+// warp w owns 8 columns and lane i row i of the chunk, so every load of a partial is
+// a coalesced 128-byte line.  The loads of kMergeBatch partials are issued together
+// before they are folded in with a running maximum: the kernel is bound by load
+// latency, and this keeps the round trips per row at ceil(parts / kMergeBatch).
 // Launched as a programmatic dependent of the attention kernel: griddepcontrol.wait
 // returns once that grid has completed and its writes are visible.
 constexpr int kMergeThreads = 256;
+constexpr int kMergeCols = 8;   // columns per warp
+constexpr int kMergeBatch = 4;  // partials in flight per thread
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads, 4) block_attn_merge_kernel(const AttnArgs a) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    constexpr int kCols = D / 8;
-    const int p = blockIdx.x >> 3, chunk = blockIdx.x & 7;
+    constexpr int kColChunks = D / (8 * kMergeCols);
+    const int p = blockIdx.x / (8 * kColChunks);
+    const int chunk = (blockIdx.x / kColChunks) & 7, cc = blockIdx.x % kColChunks;
     const int2 cs = a.pair_split[p];
     if (cs.x == cs.y) return;  // finished inside one CTA
     const int rg = p % a.NRG;
@@ -823,41 +828,49 @@ __global__ void __launch_bounds__(kMergeThreads, 4) block_attn_merge_kernel(cons
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int rl = chunk * 32 + lane;
     if (rl >= rows) return;
+    const int col0 = (cc * 8 + warp) * kMergeCols;
+    // the partial of CTA c for pair p sits in slot c + p
     const float2 *mlp = a.part_ml + static_cast<size_t>(p) * kRows + rl;  // + c * kRows
-    const float *op = a.part_o + (static_cast<size_t>(p) * D + kCols * warp) * kRows + rl;
+    const float *op = a.part_o + (static_cast<size_t>(p) * D + col0) * kRows + rl;
     float M = -INFINITY, den = 0.f;
-    float acc[kCols];
+    float acc[kMergeCols];
 #pragma unroll
-    for (int e = 0; e < kCols; ++e) acc[e] = 0.f;
-#pragma unroll 2
-    for (int c = cs.x; c <= cs.y; ++c) {
-        const float2 ml = __ldcg(mlp + static_cast<size_t>(c) * kRows);
-        const float *src = op + static_cast<size_t>(c) * D * kRows;
-        float v[kCols];
+    for (int e = 0; e < kMergeCols; ++e) acc[e] = 0.f;
+    for (int c0 = cs.x; c0 <= cs.y; c0 += kMergeBatch) {
+        float2 ml[kMergeBatch];
+        float v[kMergeBatch][kMergeCols];
 #pragma unroll
-        for (int e = 0; e < kCols; ++e) v[e] = __ldcg(src + e * kRows);
-        const float Mn = fmaxf(M, ml.x);
-        const float so = ex2_approx(M - Mn), w = ex2_approx(ml.x - Mn) * ml.y;
-        M = Mn;
-        den = den * so + w;
+        for (int i = 0; i < kMergeBatch; ++i) {
+            const int c = min(c0 + i, cs.y);  // past the last partial: a repeat, not folded in
+            ml[i] = __ldcg(mlp + static_cast<size_t>(c) * kRows);
+            const float *src = op + static_cast<size_t>(c) * D * kRows;
 #pragma unroll
-        for (int e = 0; e < kCols; ++e) acc[e] = acc[e] * so + w * v[e];
+            for (int e = 0; e < kMergeCols; ++e) v[i][e] = __ldcg(src + e * kRows);
+        }
+#pragma unroll
+        for (int i = 0; i < kMergeBatch; ++i) {
+            if (c0 + i <= cs.y) {
+                const float Mn = fmaxf(M, ml[i].x);
+                const float so = ex2_approx(M - Mn), w = ex2_approx(ml[i].x - Mn) * ml[i].y;
+                M = Mn;
+                den = den * so + w;
+#pragma unroll
+                for (int e = 0; e < kMergeCols; ++e) acc[e] = acc[e] * so + w * v[i][e];
+            }
+        }
     }
     const float inv = 1.f / den;
     const int rr = rg * kRows + rl;
     const int bg = p / a.NRG, g = bg % a.Hkv, b = bg / a.Hkv;
     const int sq = rr / a.G, head = g * a.G + rr % a.G;
-    uint16_t *dst = a.out + b * a.os[0] + sq * a.os[1] + head * a.os[2] + kCols * warp;
-#pragma unroll
-    for (int j = 0; j < kCols / 8; ++j) {
-        uint4 o;
-        o.x = pack_bf16x2(acc[8 * j + 0] * inv, acc[8 * j + 1] * inv);
-        o.y = pack_bf16x2(acc[8 * j + 2] * inv, acc[8 * j + 3] * inv);
-        o.z = pack_bf16x2(acc[8 * j + 4] * inv, acc[8 * j + 5] * inv);
-        o.w = pack_bf16x2(acc[8 * j + 6] * inv, acc[8 * j + 7] * inv);
-        *reinterpret_cast<uint4 *>(dst + 8 * j) = o;
-    }
-    if (warp == 0 && a.lse)
+    uint16_t *dst = a.out + b * a.os[0] + sq * a.os[1] + head * a.os[2] + col0;
+    uint4 o;
+    o.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    o.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    o.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+    o.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+    *reinterpret_cast<uint4 *>(dst) = o;
+    if (col0 == 0 && a.lse)
         a.lse[(static_cast<int64_t>(b) * a.Hq + head) * a.S + sq] = (M + __log2f(den)) * kLn2;
 }
 
@@ -1046,7 +1059,7 @@ tt_status launch(const tt_attn_desc *d, const AttnArgs &a, const void *k_ctx, co
     tt_status st2 = cuda_status(cudaGetLastError(), "tt_block_attn launch");
     if (st2 != TT_OK) return st2;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(a.npairs) * 8);
+    cfg.gridDim = dim3(static_cast<unsigned>(a.npairs) * 8 * (D / (8 * kMergeCols)));
     cfg.blockDim = dim3(kMergeThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
