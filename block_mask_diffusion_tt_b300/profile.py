@@ -7,43 +7,101 @@ device footprint of one layer (a few hundred MB) rather than the whole step.
 
 `attn` runs `tt_block_attn` on one layer's block queries and context K/V;
 `unmask` runs `tt_confidence_unmask` on a step where every position is masked.
+
+With --time it instead times back-to-back calls with CUDA events and prints the
+mean time per call and the algorithmic bandwidth.  For attention it cycles over
+enough layers (each with its own K/V) that their caches together exceed twice the
+L2 size, so no call finds its K/V in L2.
 """
 import argparse
 
+import numpy as np
 import torch
 
 from . import synth, tt
 
+L2_BYTES = 126 * 1024 * 1024
 
-def run_attn(w: synth.Workload, n: int):
-    a = w.attn
-    g = torch.Generator(device="cuda")
-    g.manual_seed(w.seed)
 
+def _attn_layer(a, g):
     def randn(shape):
         return torch.randn(shape, generator=g, device="cuda").to(torch.bfloat16)
 
-    lens = torch.from_numpy(synth.ctx_lens_for(a, w.seed)).cuda()
     q = randn((a.B, a.S, a.Hq, a.d))
-    k_ctx, v_ctx = randn((a.B, a.Hkv, a.Lmax, a.d)), randn((a.B, a.Hkv, a.Lmax, a.d))
-    k_blk, v_blk = randn((a.B, a.S, a.Hkv, a.d)), randn((a.B, a.S, a.Hkv, a.d))
-    out = torch.empty_like(q)
-    ws = tt.Workspace(tt.block_attn_workspace_size(tt.attn_desc(q, k_ctx, v_ctx, k_blk, v_blk,
-                                                                 out)))
-    for _ in range(n):
-        tt.block_attn(q, k_ctx, v_ctx, lens, k_blk, v_blk, out=out, workspace=ws)
+    return dict(q=q, k_ctx=randn((a.B, a.Hkv, a.Lmax, a.d)), v_ctx=randn((a.B, a.Hkv, a.Lmax, a.d)),
+                k_blk=randn((a.B, a.S, a.Hkv, a.d)), v_blk=randn((a.B, a.S, a.Hkv, a.d)),
+                out=torch.empty_like(q))
 
 
-def run_unmask(w: synth.Workload, n: int):
+def attn_bytes(a, lens_np) -> int:
+    """Algorithmic bytes of one call: visible K/V, block K/V, Q and O (bf16)."""
+    kv = int(lens_np.astype(np.int64).sum()) * a.Hkv * a.d * 2 * 2
+    return kv + a.B * a.S * a.Hkv * a.d * 2 * 2 + a.B * a.S * a.Hq * a.d * 2 * 2
+
+
+def run_attn(w: synth.Workload, n: int, time_it: bool = False):
+    a = w.attn
+    g = torch.Generator(device="cuda")
+    g.manual_seed(w.seed)
+    lens_np = synth.ctx_lens_for(a, w.seed)
+    lens = torch.from_numpy(lens_np).cuda()
+    cache = a.B * a.Hkv * a.Lmax * a.d * 2 * 2
+    nl = max(2, -(-2 * L2_BYTES // cache)) if time_it else 1
+    layers = [_attn_layer(a, g) for _ in range(nl)]
+    l0 = layers[0]
+    ws = tt.Workspace(tt.block_attn_workspace_size(
+        tt.attn_desc(l0["q"], l0["k_ctx"], l0["v_ctx"], l0["k_blk"], l0["v_blk"], l0["out"])))
+
+    def call(ly):
+        tt.block_attn(ly["q"], ly["k_ctx"], ly["v_ctx"], lens, ly["k_blk"], ly["v_blk"],
+                      out=ly["out"], workspace=ws)
+
+    if not time_it:
+        for _ in range(n):
+            call(l0)
+        return None
+    for _ in range(3):
+        for ly in layers:
+            call(ly)
+    torch.cuda.synchronize()
+    rounds = max(1, -(-n // nl))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(rounds):
+        for ly in layers:
+            call(ly)
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (rounds * nl)
+    return us, attn_bytes(a, lens_np) / us / 1e3, f"{nl} layers"
+
+
+def run_unmask(w: synth.Workload, n: int, time_it: bool = False):
     a = w.attn
     logits = tt.synth_logits(w.seed, 0, a.B, a.S, w.V, w.sigma,
                              synth.spike_threshold(w.spike_p), tt.TT_BF16)
     tokens = torch.empty((a.B, a.S), dtype=torch.int32, device="cuda")
     masked = torch.empty((a.B, a.S), dtype=torch.uint8, device="cuda")
-    for _ in range(n):
+    ws = tt.Workspace(tt.confidence_unmask_workspace_size(
+        tt.unmask_desc(a.B, a.S, w.V, tt.TT_BF16, w.temperature, w.threshold, w.mask_token_id)))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)] if time_it else None
+    for i in range((3 if time_it else 0) + n):
         tt.block_init(tokens, masked, w.mask_token_id)
+        timed = time_it and i >= 3
+        if timed:
+            ev[i - 3][0].record()
         tt.confidence_unmask(logits, tokens, masked, w.temperature, w.threshold,
-                             w.mask_token_id)
+                             w.mask_token_id, workspace=ws)
+        if timed:
+            ev[i - 3][1].record()
+    if not time_it:
+        return None
+    torch.cuda.synchronize()
+    us = sum(s.elapsed_time(e) for s, e in ev) * 1e3 / n
+    # every position is masked at a block's first step: whole rows plus the state arrays
+    nbytes = a.B * a.S * w.V * 2 + a.B * a.S * (4 + 1 + 4 + 1 + 4) + a.B * 4
+    return us, nbytes / us / 1e3, "events around each call"
 
 
 def main():
@@ -51,12 +109,18 @@ def main():
     ap.add_argument("op", choices=["attn", "unmask"])
     ap.add_argument("workload", choices=sorted(synth.workloads()))
     ap.add_argument("n", type=int, nargs="?", default=4)
+    ap.add_argument("--time", action="store_true",
+                    help="time n back-to-back calls with CUDA events instead")
     args = ap.parse_args()
     tt.load()
     w = synth.workloads()[args.workload]
-    (run_attn if args.op == "attn" else run_unmask)(w, args.n)
+    res = (run_attn if args.op == "attn" else run_unmask)(w, args.n, args.time)
     torch.cuda.synchronize()
-    print("ok", args.op, w.name, args.n)
+    if res is None:
+        print("ok", args.op, w.name, args.n)
+    else:
+        us, gbs, how = res
+        print(f"{args.op} {w.name}: {us:.1f} us per call, {gbs:.0f} GB/s ({how})")
 
 
 if __name__ == "__main__":
