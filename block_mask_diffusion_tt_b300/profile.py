@@ -9,11 +9,13 @@ device footprint of one layer (a few hundred MB) rather than the whole step.
 `unmask` runs `tt_confidence_unmask` on a step where every position is masked.
 
 With --time it instead times back-to-back calls with CUDA events and prints the
-mean time per call and the algorithmic bandwidth.  For attention it cycles over
-enough layers (each with its own K/V) that their caches together exceed twice the
-L2 size, so no call finds its K/V in L2.
+mean time per call and the algorithmic bandwidth.  The timed calls go to the C ABI
+with arguments built once, so host work does not leave the GPU idle between
+kernels.  For attention it cycles over enough layers (each with its own K/V) that
+their caches together exceed twice the L2 size, so no call finds its K/V in L2.
 """
 import argparse
+import ctypes
 
 import numpy as np
 import torch
@@ -52,24 +54,31 @@ def run_attn(w: synth.Workload, n: int, time_it: bool = False):
     ws = tt.Workspace(tt.block_attn_workspace_size(
         tt.attn_desc(l0["q"], l0["k_ctx"], l0["v_ctx"], l0["k_blk"], l0["v_blk"], l0["out"])))
 
-    def call(ly):
-        tt.block_attn(ly["q"], ly["k_ctx"], ly["v_ctx"], lens, ly["k_blk"], ly["v_blk"],
-                      out=ly["out"], workspace=ws)
-
     if not time_it:
         for _ in range(n):
-            call(l0)
+            tt.block_attn(l0["q"], l0["k_ctx"], l0["v_ctx"], lens, l0["k_blk"], l0["v_blk"],
+                          out=l0["out"], workspace=ws)
         return None
+    lib = tt.load()
+    desc = tt.attn_desc(l0["q"], l0["k_ctx"], l0["v_ctx"], l0["k_blk"], l0["v_blk"], l0["out"])
+    sp = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    argv = [(ctypes.byref(desc), tt._ptr(ly["q"]), tt._ptr(ly["k_ctx"]), tt._ptr(ly["v_ctx"]),
+             tt._ptr(lens), tt._ptr(ly["k_blk"]), tt._ptr(ly["v_blk"]), tt._ptr(ly["out"]), None,
+             ws.ptr, ws.nbytes, sp) for ly in layers]
+
+    def call(i):
+        tt.check(lib.tt_block_attn(*argv[i]))
+
     for _ in range(3):
-        for ly in layers:
-            call(ly)
+        for i in range(nl):
+            call(i)
     torch.cuda.synchronize()
     rounds = max(1, -(-n // nl))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(rounds):
-        for ly in layers:
-            call(ly)
+        for i in range(nl):
+            call(i)
     e1.record()
     torch.cuda.synchronize()
     us = e0.elapsed_time(e1) * 1e3 / (rounds * nl)
@@ -82,21 +91,31 @@ def run_unmask(w: synth.Workload, n: int, time_it: bool = False):
                              synth.spike_threshold(w.spike_p), tt.TT_BF16)
     tokens = torch.empty((a.B, a.S), dtype=torch.int32, device="cuda")
     masked = torch.empty((a.B, a.S), dtype=torch.uint8, device="cuda")
-    ws = tt.Workspace(tt.confidence_unmask_workspace_size(
-        tt.unmask_desc(a.B, a.S, w.V, tt.TT_BF16, w.temperature, w.threshold, w.mask_token_id)))
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(n)] if time_it else None
-    for i in range((3 if time_it else 0) + n):
-        tt.block_init(tokens, masked, w.mask_token_id)
-        timed = time_it and i >= 3
-        if timed:
-            ev[i - 3][0].record()
-        tt.confidence_unmask(logits, tokens, masked, w.temperature, w.threshold,
-                             w.mask_token_id, workspace=ws)
-        if timed:
-            ev[i - 3][1].record()
+    desc = tt.unmask_desc(a.B, a.S, w.V, tt.TT_BF16, w.temperature, w.threshold, w.mask_token_id)
+    ws = tt.Workspace(tt.confidence_unmask_workspace_size(desc))
     if not time_it:
+        for _ in range(n):
+            tt.block_init(tokens, masked, w.mask_token_id)
+            tt.confidence_unmask(logits, tokens, masked, w.temperature, w.threshold,
+                                 w.mask_token_id, workspace=ws)
         return None
+    lib = tt.load()
+    sp = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    conf = torch.empty((a.B, a.S), dtype=torch.float32, device="cuda")
+    now = torch.empty((a.B, a.S), dtype=torch.uint8, device="cuda")
+    remaining = torch.empty((a.B,), dtype=torch.int32, device="cuda")
+    init_args = (ctypes.byref(desc), tt._ptr(tokens), tt._ptr(masked), None, None, sp)
+    unmask_args = (ctypes.byref(desc), tt._ptr(logits), tt._ptr(tokens), tt._ptr(masked),
+                   tt._ptr(conf), tt._ptr(now), tt._ptr(remaining), 0, ws.ptr, ws.nbytes, sp)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    for i in range(3 + n):
+        tt.check(lib.tt_block_init(*init_args))
+        if i >= 3:
+            ev[i - 3][0].record()
+        tt.check(lib.tt_confidence_unmask(*unmask_args))
+        if i >= 3:
+            ev[i - 3][1].record()
     torch.cuda.synchronize()
     us = sum(s.elapsed_time(e) for s, e in ev) * 1e3 / n
     # every position is masked at a block's first step: whole rows plus the state arrays
