@@ -67,6 +67,11 @@ def recorded_traffic(workload: str):
 
 
 # ------------------------------------------------------------------ distributed plumbing
+def rank_seed(w: synth.Workload, rank: int) -> int:
+    """Seed of rank `rank`'s batch: every rank draws its own independent batch of the
+    workload (weak scaling, no data exchanged between ranks)."""
+    return w.seed + rank
+
 class Dist:
     def __init__(self, want: int, init: bool = True):
         self.world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -242,7 +247,7 @@ def run_ours(args, dist: Dist) -> dict:
     dev = f"cuda:{dist.local}"
     torch.cuda.set_device(dist.local)
     stream = torch.cuda.Stream()
-    wl = DeviceWorkload(w, seed=w.seed + dist.rank, device=dev)
+    wl = DeviceWorkload(w, seed=rank_seed(w, dist.rank), device=dev)
     a = wl.a
     clocks = ClockSampler(dist.local)
     with torch.cuda.stream(stream):
