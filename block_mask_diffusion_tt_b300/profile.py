@@ -6,7 +6,10 @@ device footprint of one layer (a few hundred MB) rather than the whole step.
     python -m block_mask_diffusion_tt_b300.profile unmask ragged16k 4
 
 `attn` runs `tt_block_attn` on one layer's block queries and context K/V;
-`unmask` runs `tt_confidence_unmask` on a step where every position is masked.
+`unmask` runs `tt_confidence_unmask` on a step where every position is masked;
+`loop` runs `tt_denoise_block_loop` with the library's synthetic logits producer
+over the sweep configuration's block sizes and thresholds (steps = S), and reports
+committed tokens/s and the steps used per block.
 
 With --time it instead times back-to-back calls with CUDA events and prints the
 mean time per call and the algorithmic bandwidth.  The timed calls go to the C ABI
@@ -123,9 +126,50 @@ def run_unmask(w: synth.Workload, n: int, time_it: bool = False):
     return us, nbytes / us / 1e3, "events around each call"
 
 
+def run_loop(w: synth.Workload, n: int, time_it: bool = False):
+    """One block per (S, gamma) of the workload's sweep (or its own S and gamma),
+    n times each; with time_it, the mean time of a block and what it committed."""
+    a = w.attn
+    ex = w.extra or {}
+    s_values = ex.get("S_values", (a.S,))
+    gammas = ex.get("gammas", (w.threshold,))
+    lines = []
+    for S in s_values:
+        ps = [synth.sweep_spike_p(k, S, ex.get("spike_p_first", w.spike_p),
+                                  ex.get("spike_p_last", w.spike_p)) for k in range(S)]
+        params = tt.synth_params(w.seed, a.B, S, w.V, tt.TT_BF16, w.sigma,
+                                 [synth.spike_threshold(p) for p in ps])
+        logits = torch.empty((a.B, S, w.V), dtype=torch.bfloat16, device="cuda")
+        tokens = torch.empty((a.B, S), dtype=torch.int32, device="cuda")
+        masked = torch.empty((a.B, S), dtype=torch.uint8, device="cuda")
+        used = torch.empty((a.B,), dtype=torch.int32, device="cuda")
+        desc = tt.unmask_desc(a.B, S, w.V, tt.TT_BF16, w.temperature, 0.5, w.mask_token_id)
+        ws = tt.Workspace(tt.denoise_block_loop_workspace_size(desc))
+        for gamma in gammas:
+            def block():
+                return tt.denoise_block_loop(a.B, S, w.V, tt.TT_BF16, w.temperature, gamma,
+                                             w.mask_token_id, S, tokens, masked, used,
+                                             logits_buf=logits, synth=params, workspace=ws)
+            block()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(n):
+                steps = block()
+            e1.record()
+            torch.cuda.synchronize()
+            if time_it:
+                us = e0.elapsed_time(e1) * 1e3 / n
+                mean_used = float(used.float().mean())
+                lines.append(f"S={S:2d} gamma={gamma:.2f}: {us:8.1f} us per block, "
+                             f"{a.B * S / us * 1e6:12.0f} committed tokens/s, "
+                             f"steps used per block {mean_used:.2f} (loop ran {steps})")
+    return ("\n".join(lines), None, None) if time_it else None
+
+
 def main():
     ap = argparse.ArgumentParser(description="run one op of the step n times")
-    ap.add_argument("op", choices=["attn", "unmask"])
+    ap.add_argument("op", choices=["attn", "unmask", "loop"])
     ap.add_argument("workload", choices=sorted(synth.workloads()))
     ap.add_argument("n", type=int, nargs="?", default=4)
     ap.add_argument("--time", action="store_true",
@@ -133,10 +177,13 @@ def main():
     args = ap.parse_args()
     tt.load()
     w = synth.workloads()[args.workload]
-    res = (run_attn if args.op == "attn" else run_unmask)(w, args.n, args.time)
+    run = dict(attn=run_attn, unmask=run_unmask, loop=run_loop)[args.op]
+    res = run(w, args.n, args.time)
     torch.cuda.synchronize()
     if res is None:
         print("ok", args.op, w.name, args.n)
+    elif args.op == "loop":
+        print(f"loop {w.name}:\n{res[0]}")
     else:
         us, gbs, how = res
         print(f"{args.op} {w.name}: {us:.1f} us per call, {gbs:.0f} GB/s ({how})")
