@@ -43,9 +43,11 @@ def measured_peaks() -> dict:
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             p = json.load(f)
-        return dict(hbm_gbs=float(p["hbm_gbs"]), source="measured")
+        return dict(hbm_gbs=float(p["hbm_gbs"]), bf16_tflops=float(p["bf16_tflops"]),
+                    bf16_tflops_sustained=float(p["bf16_tflops_sustained"]), source="measured")
     except Exception:
-        return dict(hbm_gbs=6400.0, source="fallback")
+        return dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0,
+                    source="fallback")
 
 
 def recorded_traffic(workload: str):
@@ -299,7 +301,13 @@ def run_ours(args, dist: Dist) -> dict:
         attn=dict(query_tokens_per_s=a.B * a.S / (attn_avg * 1e-3), hbm_gbs=achieved,
                   frac_of_measured=achieved / peaks["hbm_gbs"],
                   frac_of_8tbs=achieved / NORTH_STAR_HBM_GBS,
-                  tflops=wl.attn_flops() / (attn_avg * 1e-3) / 1e12, avg_ms=attn_avg),
+                  tflops=wl.attn_flops() / (attn_avg * 1e-3) / 1e12, avg_ms=attn_avg,
+                  # the call is co-bound: against the bf16 tensor peak (sustained, since it
+                  # is timed inside a long step), and the floor each roof sets for it
+                  frac_of_bf16_sustained=wl.attn_flops() / (attn_avg * 1e-3) / 1e12 /
+                  peaks["bf16_tflops_sustained"],
+                  floor_ms_hbm=ab / peaks["hbm_gbs"] / 1e6,
+                  floor_ms_tensor_sustained=wl.attn_flops() / peaks["bf16_tflops_sustained"] / 1e9),
         unmask=dict(positions_per_s=a.B * a.S / (unm_avg * 1e-3),
                     hbm_gbs=wl.unmask_bytes() / (unm_avg * 1e-3) / 1e9,
                     frac_of_measured=wl.unmask_bytes() / (unm_avg * 1e-3) / 1e9 / peaks["hbm_gbs"],
