@@ -53,6 +53,29 @@ def test_many_splits_one_long_sequence():
     _gpu.check_attn(synth.attn_inputs(shape, seed=5), what="long single")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_many_short_pairs_per_cta(d):
+    """300 short sequences: every CTA walks through several pairs, so Q is reloaded at
+    each segment and the two S buffers alternate across segment boundaries with odd
+    and even tile counts; some pairs are split between CTAs, some are not."""
+    rng = np.random.default_rng(11)
+    lens = [int(x) for x in rng.integers(0, 130, size=300)]
+    lens[:4] = [0, 1, 64, 129]
+    shape = synth.AttnShape(300, 16, 32, 2, d, 130, lens=lens)
+    _gpu.check_attn(synth.attn_inputs(shape, seed=12 + d), what=f"many short pairs d={d}")
+
+
+def test_running_max_grows_across_tiles():
+    """Keys whose norm grows along the prefix: later tiles raise the row maximum by far more
+    than the lazy-rescale threshold, so O in TMEM is rescaled repeatedly mid-stream."""
+    shape = synth.AttnShape(2, 16, 32, 2, 128, 1500, lens=[1500, 700])
+    inp = synth.attn_inputs(shape, seed=21)
+    k = synth.bf16_to_f32(inp["k_ctx"])
+    ramp = np.linspace(0.2, 6.0, shape.Lmax, dtype=np.float32)[None, None, :, None]
+    inp["k_ctx"] = synth.bf16_bits(k * ramp)
+    _gpu.check_attn(inp, what="growing key norms")
+
+
 def test_strided_views():
     """q taken from a fused [B,S,Hq+2Hkv,d] projection, caches inside larger buffers."""
     B, S, Hq, Hkv, d, L = 2, 16, 8, 2, 128, 200
