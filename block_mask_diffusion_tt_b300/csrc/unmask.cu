@@ -9,7 +9,7 @@
 //  * grid = (B*S rows) x (nch vocabulary chunks), 256 threads per CTA; a CTA
 //    whose row is not masked returns after one arrival (rows that are not masked
 //    cost one byte of traffic);
-//  * one pass over the chunk with 16-byte streaming loads, eight in flight per
+//  * one pass over the chunk with 16-byte streaming loads, four in flight per
 //    thread; per thread a running raw-logit maximum, its first index and
 //    sum 2^((l - max) * log2(e)/T), rescaled when the maximum grows; a vector of
 //    8 logits whose maximum lies 2^40 below the running maximum's term adds
@@ -32,7 +32,9 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kMaxS = 64;
-constexpr int kUnroll = 8;
+// Loads in flight per thread.  Four keep the kernel at 40 registers, so six CTAs fit
+// on an SM; measured faster than eight, twelve or sixteen, which fit fewer CTAs.
+constexpr int kUnroll = 4;
 // Terms 2^((l - m) k) below 2^-kSkipLog2 of the running maximum's term are not
 // added: a vector of logits whose largest element is that far below the running
 // maximum contributes nothing.  The maximum is only ever raised, so every skipped
