@@ -50,18 +50,27 @@ def measured_peaks() -> dict:
                     source="fallback")
 
 
+def code_hash(path: str) -> str:
+    """sha256 of a C/CUDA source with comments and whitespace removed, so that a
+    record taken on one version of a kernel stays valid across comment edits only."""
+    import hashlib
+    import re
+    src = open(path).read()
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return hashlib.sha256("".join(src.split()).encode()).hexdigest()
+
+
 def recorded_traffic(workload: str):
     """DRAM bytes per attention call from the committed ncu capture summary
-    (profiles/traffic.json), used only while the attention source is the one that
-    capture measured (sha256 of attn.cu); otherwise None."""
-    import hashlib
+    (profiles/traffic.json), used only while the attention source is the code that
+    capture measured (code_hash of attn.cu); otherwise None."""
     try:
         src = os.path.join(ROOT, "block_mask_diffusion_tt_b300", "csrc", "attn.cu")
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f)
         e = rec.get(workload)
-        if e and e.get("attn_cu_sha256") == sha:
+        if e and e.get("attn_cu_code_sha256") == code_hash(src):
             return e["dram_bytes_per_call"]
     except Exception:
         pass

@@ -617,9 +617,9 @@ __device__ void role_softmax(const AttnArgs &a, Sched sch, const Smem<D> &sm, ui
             ++cnt;
         }
         if (!ok) break;
-        // The next segment's Q goes into TMEM before this segment's epilogue (the last
-        // Q K^T of this segment has completed: its S was read), so the MMA warp can
-        // start on the next segment while O is read out and stored.
+        // The next segment's Q goes into shared memory before this segment's epilogue
+        // (every Q K^T of this segment has completed: the last S was read), so the MMA
+        // warp can start on the next segment while O is read out and stored.
         const bool have_next = next_mine(nxt);
         if (have_next) load_q(nxt);
         // ---- segment epilogue: O_h is final once the last P_h V is done
