@@ -9,7 +9,9 @@ device footprint of one layer (a few hundred MB) rather than the whole step.
 `unmask` runs `tt_confidence_unmask` on a step where every position is masked;
 `loop` runs `tt_denoise_block_loop` with the library's synthetic logits producer
 over the sweep configuration's block sizes and thresholds (steps = S), and reports
-committed tokens/s and the steps used per block.
+committed tokens/s and the steps used per block;
+`kvappend` runs `tt_kv_append` for every attention layer of the workload (a
+committed block of S rows joins each layer's context cache).
 
 With --time it instead times back-to-back calls with CUDA events and prints the
 mean time per call and the algorithmic bandwidth.  The timed calls go to the C ABI
@@ -167,9 +169,43 @@ def run_loop(w: synth.Workload, n: int, time_it: bool = False):
     return ("\n".join(lines), None, None) if time_it else None
 
 
+def run_kvappend(w: synth.Workload, n: int, time_it: bool = False):
+    """tt_kv_append of one committed block into the workload's attention layers; the
+    prefix lengths are reset before every call, outside the timed events."""
+    a = w.attn
+    g = torch.Generator(device="cuda")
+    g.manual_seed(w.seed)
+
+    def randn(shape):
+        return torch.randn(shape, generator=g, device="cuda").to(torch.bfloat16)
+
+    L = w.n_layers
+    kc = [randn((a.B, a.Hkv, a.Lmax, a.d)) for _ in range(L)]
+    vc = [randn((a.B, a.Hkv, a.Lmax, a.d)) for _ in range(L)]
+    kb = [randn((a.B, a.S, a.Hkv, a.d)) for _ in range(L)]
+    vb = [randn((a.B, a.S, a.Hkv, a.d)) for _ in range(L)]
+    lens0 = torch.from_numpy(np.minimum(synth.ctx_lens_for(a, w.seed), a.Lmax - a.S)).cuda()
+    lens = lens0.clone()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    for i in range(3 + n):
+        lens.copy_(lens0)
+        if i >= 3:
+            ev[i - 3][0].record()
+        tt.kv_append(kc, vc, lens, kb, vb)
+        if i >= 3:
+            ev[i - 3][1].record()
+    torch.cuda.synchronize()
+    if not time_it:
+        return None
+    us = sum(s.elapsed_time(e) for s, e in ev) * 1e3 / n
+    nbytes = 2 * (L * 2 * a.B * a.S * a.Hkv * a.d * 2)  # each block row read once, written once
+    return us, nbytes / us / 1e3, f"{L} layers, events around each call"
+
+
 def main():
     ap = argparse.ArgumentParser(description="run one op of the step n times")
-    ap.add_argument("op", choices=["attn", "unmask", "loop"])
+    ap.add_argument("op", choices=["attn", "unmask", "loop", "kvappend"])
     ap.add_argument("workload", choices=sorted(synth.workloads()))
     ap.add_argument("n", type=int, nargs="?", default=4)
     ap.add_argument("--time", action="store_true",
@@ -177,7 +213,7 @@ def main():
     args = ap.parse_args()
     tt.load()
     w = synth.workloads()[args.workload]
-    run = dict(attn=run_attn, unmask=run_unmask, loop=run_loop)[args.op]
+    run = dict(attn=run_attn, unmask=run_unmask, loop=run_loop, kvappend=run_kvappend)[args.op]
     res = run(w, args.n, args.time)
     torch.cuda.synchronize()
     if res is None:

@@ -21,6 +21,7 @@ TT_OK, TT_ERR_INVALID_ARG, TT_ERR_UNSUPPORTED, TT_ERR_WORKSPACE = 0, 1, 2, 3
 TT_ERR_CUDA, TT_ERR_TIMEOUT, TT_ERR_CALLBACK, TT_ERR_INTERNAL = 4, 5, 6, 7
 TT_F32, TT_BF16 = 0, 1
 SYNTH_MAX_STEPS = 256
+KV_MAX_LAYERS = 16
 
 _i32 = ctypes.c_int32
 _p = ctypes.c_void_p
@@ -51,6 +52,11 @@ class SynthParams(ctypes.Structure):
     _fields_ = [("seed", ctypes.c_uint64), ("B", _i32), ("S", _i32), ("V", _i32),
                 ("dtype", ctypes.c_int), ("sigma", ctypes.c_float),
                 ("spike_threshold", ctypes.c_uint64 * SYNTH_MAX_STEPS)]
+
+
+class KvDesc(ctypes.Structure):
+    _fields_ = [("B", _i32), ("S", _i32), ("Hkv", _i32), ("d", _i32), ("Lmax", _i32),
+                ("n_layers", _i32), ("ctx_strides", _i64x4), ("blk_strides", _i64x4)]
 
 
 LOGITS_FN = ctypes.CFUNCTYPE(ctypes.c_int, _p, _i32, _p, _p, _p, _p)
@@ -86,6 +92,7 @@ def load(path: str = LIB_PATH):
         "tt_synth_logits": (ctypes.c_int, [ctypes.c_uint64, _i32, _i32, _i32, _i32, ctypes.c_int,
                                            ctypes.c_float, ctypes.c_uint64, _p, _p]),
         "tt_synth_logits_producer": (ctypes.c_int, [_p, _i32, _p, _p, _p, _p]),
+        "tt_kv_append": (ctypes.c_int, [ctypes.POINTER(KvDesc), _p, _p, _p, _p, _p, _p, _p, _p]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -344,6 +351,45 @@ def denoise_block_loop(B: int, S: int, V: int, logits_dtype: int, temperature: f
     return int(steps_run.value)
 
 
+# ------------------------------------------------------------------ block append
+def kv_append(k_ctx: list, v_ctx: list, ctx_lens, k_blk: list, v_blk: list, active=None,
+              overflow=None, stream=None):
+    """Appends the committed block's K/V of every layer to its cache (tt_kv_append).
+
+    k_ctx/v_ctx: per layer bf16 [B,Hkv,Lmax,d]; k_blk/v_blk: per layer bf16 [B,S,Hkv,d];
+    ctx_lens int32[B] is advanced in place; active uint8[B] or None; overflow int32[1]
+    or None counts sequences whose block did not fit.
+    """
+    n = len(k_ctx)
+    if not (n == len(v_ctx) == len(k_blk) == len(v_blk)) or not 1 <= n <= KV_MAX_LAYERS:
+        raise ValueError(f"need 1..{KV_MAX_LAYERS} layers, the same count in each list")
+    for lst, name in ((k_ctx, "k_ctx"), (v_ctx, "v_ctx"), (k_blk, "k_blk"), (v_blk, "v_blk")):
+        for t in lst:
+            _need(t, name, torch.bfloat16, 4)
+    _need(ctx_lens, "ctx_lens", torch.int32, 1)
+    if active is not None:
+        _need(active, "active", torch.uint8, 1)
+    if overflow is not None:
+        _need(overflow, "overflow", torch.int32, 1)
+    B, Hkv, Lmax, d = k_ctx[0].shape
+    S = k_blk[0].shape[1]
+    for lst in (k_ctx, v_ctx):
+        for t in lst:
+            if tuple(t.shape) != (B, Hkv, Lmax, d) or t.stride() != k_ctx[0].stride():
+                raise ValueError("every cache must have the first cache's shape and strides")
+    for lst in (k_blk, v_blk):
+        for t in lst:
+            if tuple(t.shape) != (B, S, Hkv, d) or t.stride() != k_blk[0].stride():
+                raise ValueError("every block must have shape [B,S,Hkv,d] and equal strides")
+    desc = KvDesc(B=B, S=S, Hkv=Hkv, d=d, Lmax=Lmax, n_layers=n)
+    desc.ctx_strides = _i64x4(*k_ctx[0].stride())
+    desc.blk_strides = _i64x4(*k_blk[0].stride())
+    arr = ctypes.c_void_p * n
+    ptrs = [arr(*[t.data_ptr() for t in lst]) for lst in (k_ctx, v_ctx, k_blk, v_blk)]
+    check(load().tt_kv_append(ctypes.byref(desc), ptrs[0], ptrs[1], _ptr(ctx_lens), ptrs[2],
+                              ptrs[3], _ptr(active), _ptr(overflow), _stream(stream)))
+
+
 def exported_symbols() -> list:
     """Names of the entry points this binding expects libtt.so to export."""
     return ["tt_status_string", "tt_last_error", "tt_abi_version", "tt_workspace_zero",
@@ -352,4 +398,4 @@ def exported_symbols() -> list:
             "tt_confidence_unmask_workspace_size",
             "tt_confidence_unmask", "tt_block_init", "tt_denoise_block_loop_workspace_size",
             "tt_denoise_block_loop",
-            "tt_synth_logits", "tt_synth_logits_producer"]
+            "tt_synth_logits", "tt_synth_logits_producer", "tt_kv_append"]

@@ -320,6 +320,47 @@ tt_status tt_synth_logits_producer(void *user, int32_t step, const int32_t *toke
                                    const uint8_t *is_masked, void *logits_out,
                                    tt_stream_t stream);
 
+/* ---------------------------------------------------------------- block append
+ *
+ * Once every position of a block is committed, the block becomes clean context:
+ * the context tower takes it in and the next block attends to a prefix S tokens
+ * longer (dothoosh.com, "فرآیند انتشار در برابر رمزگشایی متوالی در مدل جدید
+ * انویدیا", section "two-tower mechanism": blocks are generated one after another,
+ * each attending causally to the earlier clean blocks).  tt_kv_append writes the
+ * block's K/V, per layer, into that layer's context cache after the prefix and
+ * advances the prefix length; the K/V values themselves come from the caller
+ * (the context tower's forward on the committed tokens, outside this library).
+ */
+#define TT_KV_MAX_LAYERS 16
+
+typedef struct {
+    int32_t B, S, Hkv, d, Lmax;
+    int32_t n_layers;        /* 1..TT_KV_MAX_LAYERS */
+    int64_t ctx_strides[4];  /* every layer's k_ctx / v_ctx [B, Hkv, Lmax, d] */
+    int64_t blk_strides[4];  /* every layer's k_blk / v_blk [B, S, Hkv, d] */
+} tt_kv_desc;
+
+/*
+ * For every layer l < n_layers and sequence b taking part (active == NULL, or
+ * active[b] != 0), with L_b = ctx_lens[b] on entry and L_b + S <= Lmax:
+ *   k_ctx[l][b, g, L_b + s, :] = k_blk[l][b, s, g, :]   for s < S, g < Hkv,
+ * the same for V, then ctx_lens[b] = L_b + S.  Bytes are copied unchanged.
+ *   k_ctx, v_ctx  host arrays of n_layers device pointers, bf16; rows of the
+ *                 cache other than [L_b, L_b + S) are not touched.
+ *   ctx_lens      device int32[B], updated in place.
+ *   k_blk, v_blk  host arrays of n_layers device pointers, bf16.
+ *   active        device uint8[B] or NULL (every sequence).
+ *   overflow      device int32 or NULL: incremented once for every sequence that
+ *                 takes part but has L_b < 0 or L_b + S > Lmax; such a sequence's
+ *                 cache and length are left unchanged.
+ * Strides are in elements, positive multiples of 8 with the innermost one 1, and
+ * every pointer 16-byte aligned; d is a multiple of 8 up to 512.  One launch; the
+ * call returns once it is enqueued.
+ */
+tt_status tt_kv_append(const tt_kv_desc *desc, void *const *k_ctx, void *const *v_ctx,
+                       int32_t *ctx_lens, const void *const *k_blk, const void *const *v_blk,
+                       const uint8_t *active, int32_t *overflow, tt_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

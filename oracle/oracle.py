@@ -167,3 +167,42 @@ def block_loop(B: int, S: int, logits_fn: Callable[[int], np.ndarray], dtype: st
         ambiguous += int(r["ambiguous"].sum())
     return dict(tokens=tokens, is_masked=masked, steps_used=steps_used,
                 committed_step=committed_step, ambiguous=ambiguous)
+
+
+def kv_append(k_ctx: list, v_ctx: list, ctx_lens, k_blk: list, v_blk: list,
+              active=None) -> dict:
+    """Makes a committed block part of the context of every layer.
+
+    For sequence b taking part (``active`` is None or active[b] != 0) with prefix
+    length L_b = ctx_lens[b] and L_b + S <= Lmax: the S block rows of layer l, KV
+    head g, are written after the prefix, cache row L_b + s <- block row s, and the
+    prefix length becomes L_b + S.  Any other sequence keeps its cache and length;
+    one taking part that does not fit is counted in ``overflow``.  Follows the
+    block-by-block mechanism of the dothoosh.com article (section "two-tower
+    mechanism"): each clean block becomes context for the next one.
+
+    Caches are [B, Hkv, Lmax, d] and blocks [B, S, Hkv, d] per layer, copied as
+    they are (any dtype).  Returns new caches, lengths and the overflow count.
+    """
+    lens = np.asarray(ctx_lens).astype(np.int64)
+    B = lens.shape[0]
+    S = k_blk[0].shape[1]
+    Lmax = k_ctx[0].shape[2]
+    out_k = [np.array(k, copy=True) for k in k_ctx]
+    out_v = [np.array(v, copy=True) for v in v_ctx]
+    new_lens = np.array(ctx_lens, dtype=np.int32, copy=True)
+    overflow = 0
+    for b in range(B):
+        if active is not None and not active[b]:
+            continue
+        L = int(lens[b])
+        if L < 0 or L + S > Lmax:
+            overflow += 1
+            continue
+        for layer in range(len(k_ctx)):
+            for s in range(S):
+                for g in range(k_blk[layer].shape[2]):
+                    out_k[layer][b, g, L + s, :] = k_blk[layer][b, s, g, :]
+                    out_v[layer][b, g, L + s, :] = v_blk[layer][b, s, g, :]
+        new_lens[b] = L + S
+    return dict(k_ctx=out_k, v_ctx=out_v, ctx_lens=new_lens, overflow=overflow)

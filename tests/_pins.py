@@ -453,4 +453,85 @@ LOOP_CHECKS = [check_loop_defaults_from_pages, check_loop_gamma_zero_one_step,
                check_loop_gamma_above_one_s_steps, check_loop_last_step_forces_commit,
                check_loop_monotone_and_complete, check_loop_resume_bit_exact]
 
-ALL_CHECKS = ATTN_CHECKS + UNMASK_CHECKS + LOOP_CHECKS
+# ------------------------------------------------------------------ block append
+def _kv_case(seed, B=3, S=4, Hkv=2, d=8, Lmax=12, lens=(0, 5, 8), layers=2):
+    rng = np.random.default_rng(seed)
+    bits = lambda shape: synth.bf16_bits(rng.standard_normal(shape).astype(np.float32))  # noqa: E731
+    kc = [bits((B, Hkv, Lmax, d)) for _ in range(layers)]
+    vc = [bits((B, Hkv, Lmax, d)) for _ in range(layers)]
+    kb = [bits((B, S, Hkv, d)) for _ in range(layers)]
+    vb = [bits((B, S, Hkv, d)) for _ in range(layers)]
+    return kc, vc, np.array(lens, np.int32), kb, vb
+
+
+def kv_append_then_attend(lib, append_fn=None):
+    """A block appended to the context, then the next block attending over it, equals torch
+    float64 attention over keys concatenated independently: prefix rows, the appended block's
+    rows (head-major), the new block's rows."""
+    append_fn = append_fn or oracle.kv_append
+    kc, vc, lens, kb, vb = _kv_case(31, lens=(0, 5, 7))
+    B, S, Hkv, d = kb[0].shape
+    r = append_fn(kc, vc, lens, kb, vb)
+    rng = np.random.default_rng(32)
+    Hq = 2 * Hkv
+    q = synth.bf16_bits(rng.standard_normal((B, S, Hq, d)).astype(np.float32))
+    ky = synth.bf16_bits(rng.standard_normal((B, S, Hkv, d)).astype(np.float32))
+    vy = synth.bf16_bits(rng.standard_normal((B, S, Hkv, d)).astype(np.float32))
+    for layer in range(len(kc)):
+        got, _ = oracle.block_attn(q, r["k_ctx"][layer], r["v_ctx"][layer], r["ctx_lens"], ky, vy,
+                                   lib=lib)
+        for b in range(B):
+            L = int(lens[b])
+            keys = np.concatenate([f64(kc[layer][b, :, :L, :]),
+                                   f64(kb[layer][b]).transpose(1, 0, 2),
+                                   f64(ky[b]).transpose(1, 0, 2)], axis=1)
+            vals = np.concatenate([f64(vc[layer][b, :, :L, :]),
+                                   f64(vb[layer][b]).transpose(1, 0, 2),
+                                   f64(vy[b]).transpose(1, 0, 2)], axis=1)
+            qt = torch.from_numpy(f64(q[b]).transpose(1, 0, 2).copy())[None]
+            kt = torch.from_numpy(keys).repeat_interleave(Hq // Hkv, dim=0)[None]
+            vt = torch.from_numpy(vals).repeat_interleave(Hq // Hkv, dim=0)[None]
+            want = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt)[0].numpy()
+            assert np.abs(got[b] - want.transpose(1, 0, 2)).max() < 1e-9, (layer, b)
+    assert r["ctx_lens"].tolist() == [L + S for L in lens.tolist()] and r["overflow"] == 0
+
+
+def check_kv_append_then_attend_matches_library(lib):
+    kv_append_then_attend(lib)
+
+
+def check_kv_two_appends_equal_one_double_block(lib):
+    kc, vc, lens, kb, vb = _kv_case(33, S=3, Lmax=14, lens=(0, 2, 8))
+    _, _, _, kb2, vb2 = _kv_case(34, S=3, Lmax=14, lens=(0, 2, 8))
+    a = oracle.kv_append(kc, vc, lens, kb, vb)
+    a = oracle.kv_append(a["k_ctx"], a["v_ctx"], a["ctx_lens"], kb2, vb2)
+    kbb = [np.concatenate([x, y], axis=1) for x, y in zip(kb, kb2)]
+    vbb = [np.concatenate([x, y], axis=1) for x, y in zip(vb, vb2)]
+    b = oracle.kv_append(kc, vc, lens, kbb, vbb)
+    for layer in range(len(kc)):
+        assert np.array_equal(a["k_ctx"][layer], b["k_ctx"][layer])
+        assert np.array_equal(a["v_ctx"][layer], b["v_ctx"][layer])
+    assert np.array_equal(a["ctx_lens"], b["ctx_lens"])
+
+
+def check_kv_untouched_outside_the_block(lib):
+    # lengths 0, 8 (fits exactly: 8 + 4 = Lmax), 9 (does not fit), -1 (invalid), 3 (inactive)
+    kc, vc, lens, kb, vb = _kv_case(35, B=5, Lmax=12, lens=(0, 8, 9, -1, 3))
+    active = np.array([1, 1, 1, 1, 0], np.uint8)
+    r = oracle.kv_append(kc, vc, lens, kb, vb, active=active)
+    assert r["overflow"] == 2
+    assert r["ctx_lens"].tolist() == [4, 12, 9, -1, 3]
+    S = kb[0].shape[1]
+    for layer in range(len(kc)):
+        for b, L in enumerate(lens.tolist()):
+            written = L + S if r["ctx_lens"][b] != L else L
+            keep = np.ones(kc[layer].shape[2], bool)
+            keep[max(L, 0):written] = False
+            assert np.array_equal(r["k_ctx"][layer][b][:, keep], kc[layer][b][:, keep])
+            assert np.array_equal(r["v_ctx"][layer][b][:, keep], vc[layer][b][:, keep])
+
+
+KV_CHECKS = [check_kv_append_then_attend_matches_library, check_kv_two_appends_equal_one_double_block,
+             check_kv_untouched_outside_the_block]
+
+ALL_CHECKS = ATTN_CHECKS + UNMASK_CHECKS + LOOP_CHECKS + KV_CHECKS

@@ -147,3 +147,42 @@ def test_synth_rejects_bad_arguments(lib):
     assert lib.tt_synth_logits(0, -1, 1, 16, 1024, 1, 2.0, 0, None, None) == tt.TT_ERR_INVALID_ARG
     assert lib.tt_synth_logits(0, 0, 1, 16, 1024, 1, -2.0, 0, None, None) == tt.TT_ERR_INVALID_ARG
     assert lib.tt_synth_logits(0, 0, 1, 16, 1024, 1, 2.0, 0, None, None) == tt.TT_ERR_INVALID_ARG
+
+
+def _kv_desc(**kw):
+    base = dict(B=2, S=16, Hkv=2, d=128, Lmax=64, n_layers=2)
+    base.update(kw)
+    desc = tt.KvDesc(**base)
+    desc.ctx_strides = tt._i64x4(2 * 64 * 128, 64 * 128, 128, 1)
+    desc.blk_strides = tt._i64x4(16 * 2 * 128, 2 * 128, 128, 1)
+    return desc
+
+
+def _kv_call(lib, desc, ptr=None, n=2):
+    arr = (ctypes.c_void_p * max(n, 1))(*([ptr] * max(n, 1)))
+    lens = ctypes.c_void_p(ptr) if ptr else None
+    return lib.tt_kv_append(ctypes.byref(desc) if desc is not None else None, arr, arr, lens, arr,
+                            arr, None, None, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(S=0), tt.TT_ERR_INVALID_ARG), (dict(Hkv=0), tt.TT_ERR_INVALID_ARG),
+    (dict(B=-1), tt.TT_ERR_INVALID_ARG), (dict(Lmax=-1), tt.TT_ERR_INVALID_ARG),
+    (dict(n_layers=0), tt.TT_ERR_INVALID_ARG), (dict(n_layers=17), tt.TT_ERR_INVALID_ARG),
+    (dict(d=12), tt.TT_ERR_UNSUPPORTED), (dict(d=1024), tt.TT_ERR_UNSUPPORTED),
+])
+def test_kv_append_rejects_bad_desc(lib, kw, status):
+    assert _kv_call(lib, _kv_desc(**kw)) == status
+
+
+def test_kv_append_rejects_bad_strides_and_pointers(lib):
+    d = _kv_desc()
+    d.ctx_strides = tt._i64x4(2 * 64 * 128, 64 * 128, 128, 2)
+    assert _kv_call(lib, d) == tt.TT_ERR_UNSUPPORTED  # innermost stride must be 1
+    d = _kv_desc()
+    d.blk_strides = tt._i64x4(16 * 2 * 128, 2 * 128, 100, 1)
+    assert _kv_call(lib, d) == tt.TT_ERR_UNSUPPORTED  # not a multiple of 8 elements
+    assert _kv_call(lib, None) == tt.TT_ERR_INVALID_ARG
+    assert _kv_call(lib, _kv_desc()) == tt.TT_ERR_INVALID_ARG  # null pointers
+    assert _kv_call(lib, _kv_desc(), ptr=0x100008) == tt.TT_ERR_INVALID_ARG  # not 16-byte aligned
+    assert _kv_call(lib, _kv_desc(B=0)) == tt.TT_OK  # nothing to do: no launch

@@ -36,3 +36,24 @@ def test_ambiguity_flag_marks_only_fragile_decisions(lib):
     r = oracle.confidence_unmask(near, "f32", 1.0, 0.99, 3, np.full((1, 2), 3, np.int32),
                                  np.ones((1, 2), np.uint8), lib=lib)
     assert r["ambiguous"].tolist() == [[1, 1]]
+
+
+def _append_one_row_late(k_ctx, v_ctx, ctx_lens, k_blk, v_blk, active=None):
+    lens = np.asarray(ctx_lens) + 1  # planted mistake: the block lands one row after the prefix
+    r = oracle.kv_append(k_ctx, v_ctx, lens, k_blk, v_blk, active)
+    r["ctx_lens"] = np.asarray(ctx_lens, np.int32) + k_blk[0].shape[1]
+    return r
+
+
+def _append_heads_and_rows_swapped(k_ctx, v_ctx, ctx_lens, k_blk, v_blk, active=None):
+    # planted mistake: block [B,S,Hkv,d] read as if it were [B,Hkv,S,d]
+    sw = lambda t: np.ascontiguousarray(t.reshape(t.shape[0], t.shape[2], t.shape[1], t.shape[3])  # noqa: E731
+                                        .transpose(0, 2, 1, 3))
+    return oracle.kv_append(k_ctx, v_ctx, ctx_lens, [sw(x) for x in k_blk],
+                            [sw(x) for x in v_blk], active)
+
+
+@pytest.mark.parametrize("mutant", [_append_one_row_late, _append_heads_and_rows_swapped])
+def test_kv_append_pin_catches_planted_mistakes(lib, mutant):
+    with pytest.raises(AssertionError):
+        _pins.kv_append_then_attend(lib, append_fn=mutant)
