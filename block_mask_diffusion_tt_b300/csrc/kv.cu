@@ -7,16 +7,17 @@
 // [L_b, L_b + S) of that layer's cache and the prefix length grows by S.
 //
 // One CTA per sequence b: it reads L_b once, copies every layer's K and V rows as
-// 16-byte vectors (coalesced on both sides: a row is d contiguous elements), then
-// writes L_b + S.  Only CTA b touches ctx_lens[b], so one launch needs no ordering
-// between CTAs.  A sequence that is not active, or whose block would not fit under
+// 16-byte vectors (coalesced on both sides: a row is d contiguous elements), with
+// kKvUnroll loads in flight per thread before their stores, then writes L_b + S.
+// Only CTA b touches ctx_lens[b], so one launch needs no ordering between CTAs.  A sequence that is not active, or whose block would not fit under
 // Lmax, is left as it is; the second case is counted in a device word.
 #include "common.cuh"
 
 namespace tt {
 namespace {
 
-constexpr int kKvThreads = 256;
+constexpr int kKvThreads = 1024;
+constexpr int kKvUnroll = 4;
 
 struct KvArgs {
     const uint16_t *kb[TT_KV_MAX_LAYERS];
@@ -47,18 +48,31 @@ __global__ void __launch_bounds__(kKvThreads) kv_append_kernel(const KvArgs a) {
     const int vpr = a.d / 8;  // 16-byte vectors per row
     const int per_kv = a.S * a.Hkv * vpr;
     const int total = a.nl * 2 * per_kv;
-    for (int i = threadIdx.x; i < total; i += kKvThreads) {
-        const int l = i / (2 * per_kv);
-        const int r = i - l * 2 * per_kv;
-        const int kv = r / per_kv;
-        const int r2 = r - kv * per_kv;
-        const int s = r2 / (a.Hkv * vpr);
-        const int g = (r2 / vpr) % a.Hkv;
-        const int v = r2 % vpr;
-        const uint16_t *src = (kv ? a.vb[l] : a.kb[l]) + b * a.bs[0] + s * a.bs[1] + g * a.bs[2] + 8 * v;
-        uint16_t *dst = (kv ? a.vc[l] : a.kc[l]) + b * a.cs[0] + g * a.cs[1] +
-                        static_cast<int64_t>(L + s) * a.cs[2] + 8 * v;
-        *reinterpret_cast<uint4 *>(dst) = __ldcs(reinterpret_cast<const uint4 *>(src));
+    for (int i0 = threadIdx.x; i0 < total; i0 += kKvUnroll * kKvThreads) {
+        uint4 val[kKvUnroll];
+        uint16_t *dst[kKvUnroll];
+#pragma unroll
+        for (int u = 0; u < kKvUnroll; ++u) {
+            const int i = i0 + u * kKvThreads;
+            dst[u] = nullptr;
+            if (i < total) {
+                const int l = i / (2 * per_kv);
+                const int r = i - l * 2 * per_kv;
+                const int kv = r / per_kv;
+                const int r2 = r - kv * per_kv;
+                const int s = r2 / (a.Hkv * vpr);
+                const int g = (r2 / vpr) % a.Hkv;
+                const int v = r2 % vpr;
+                const uint16_t *src =
+                    (kv ? a.vb[l] : a.kb[l]) + b * a.bs[0] + s * a.bs[1] + g * a.bs[2] + 8 * v;
+                dst[u] = (kv ? a.vc[l] : a.kc[l]) + b * a.cs[0] + g * a.cs[1] +
+                         static_cast<int64_t>(L + s) * a.cs[2] + 8 * v;
+                val[u] = __ldcs(reinterpret_cast<const uint4 *>(src));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kKvUnroll; ++u)
+            if (dst[u]) *reinterpret_cast<uint4 *>(dst[u]) = val[u];
     }
     __syncthreads();
     if (threadIdx.x == 0) a.lens[b] = L + a.S;

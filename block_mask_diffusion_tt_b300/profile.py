@@ -170,8 +170,12 @@ def run_loop(w: synth.Workload, n: int, time_it: bool = False):
 
 
 def run_kvappend(w: synth.Workload, n: int, time_it: bool = False):
-    """tt_kv_append of one committed block into the workload's attention layers; the
-    prefix lengths are reset before every call, outside the timed events."""
+    """tt_kv_append of one committed block into every attention layer of the workload.
+
+    With time_it, n appends are captured in a CUDA graph and the replay is timed with
+    CUDA events: a call enqueues in more time than the kernel takes, so timing the
+    calls from the host would measure the host.  Each append lands S rows further on
+    (the lengths start low enough for all n), so every call moves the same bytes."""
     a = w.attn
     g = torch.Generator(device="cuda")
     g.manual_seed(w.seed)
@@ -184,23 +188,33 @@ def run_kvappend(w: synth.Workload, n: int, time_it: bool = False):
     vc = [randn((a.B, a.Hkv, a.Lmax, a.d)) for _ in range(L)]
     kb = [randn((a.B, a.S, a.Hkv, a.d)) for _ in range(L)]
     vb = [randn((a.B, a.S, a.Hkv, a.d)) for _ in range(L)]
-    lens0 = torch.from_numpy(np.minimum(synth.ctx_lens_for(a, w.seed), a.Lmax - a.S)).cuda()
+    room = a.Lmax - (n + 1) * a.S
+    if room < 0:
+        raise ValueError(f"Lmax={a.Lmax} has no room for {n} appends of {a.S} rows")
+    lens0 = torch.from_numpy(np.minimum(synth.ctx_lens_for(a, w.seed), room)).cuda()
     lens = lens0.clone()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(n)]
-    for i in range(3 + n):
-        lens.copy_(lens0)
-        if i >= 3:
-            ev[i - 3][0].record()
-        tt.kv_append(kc, vc, lens, kb, vb)
-        if i >= 3:
-            ev[i - 3][1].record()
-    torch.cuda.synchronize()
     if not time_it:
+        for _ in range(n):
+            tt.kv_append(kc, vc, lens, kb, vb)
         return None
-    us = sum(s.elapsed_time(e) for s, e in ev) * 1e3 / n
+    tt.kv_append(kc, vc, lens, kb, vb)  # warm-up outside the graph
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(n):
+            tt.kv_append(kc, vc, lens, kb, vb)
+    lens.copy_(lens0)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / n
+    moved = int((lens - lens0).min().item())
+    assert moved == n * a.S, f"appends in the graph moved lengths by {moved}"
     nbytes = 2 * (L * 2 * a.B * a.S * a.Hkv * a.d * 2)  # each block row read once, written once
-    return us, nbytes / us / 1e3, f"{L} layers, events around each call"
+    return us, nbytes / us / 1e3, f"{L} layers, {n} calls in one CUDA graph"
 
 
 def main():
