@@ -22,7 +22,6 @@ import ctypes
 import json
 import math
 import os
-import subprocess
 import sys
 import time
 from typing import Optional
@@ -117,56 +116,97 @@ class Dist:
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """Samples the GPU's SM clock, power and clock-event reasons during the timed region.
 
-    def __init__(self, local_rank: int):
-        self.proc = None
-        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
-        ids = [v.strip() for v in vis.split(",") if v.strip()]
-        gpu_index = ids[local_rank] if local_rank < len(ids) else str(local_rank)
-        self.path = os.path.join("/tmp", f"tt_clocks_{os.getpid()}.csv")
+    Read-only NVML queries (nvidia-ml-py) from a background thread, about one per
+    millisecond, so a timed region of a few milliseconds still gets samples; if NVML
+    cannot be used the record says why.  `mark_start()` and `mark_end()` bracket the
+    timed region; only samples taken between them count."""
+    REASONS = (("hw_slowdown", 0x8), ("hw_thermal_slowdown", 0x40),
+               ("sw_thermal_slowdown", 0x20), ("sw_power_cap", 0x4))
+
+    def __init__(self, device_index: int):
+        import threading
+        self.samples = []  # (t, sm_mhz, power_w, reasons bitmask)
+        self.t0 = self.t1 = None
+        self.err = None
+        self.stop_ev = threading.Event()
+        self.ready = threading.Event()
+        self.max_mhz = None
         try:
-            self.out = open(self.path, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.out,
-                stderr=subprocess.DEVNULL)
+            import pynvml
+            pynvml.nvmlInit()
+            self.nvml = pynvml
+            self.handle = self._handle(device_index)
+            self.max_mhz = float(pynvml.nvmlDeviceGetMaxClockInfo(self.handle,
+                                                                  pynvml.NVML_CLOCK_SM))
+        except Exception as e:  # no NVML: nothing to sample
+            self.nvml, self.err = None, f"nvml unavailable: {e}"
+            self.ready.set()
+            return
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+        self.ready.wait(5.0)
+
+    def _handle(self, device_index: int):
+        nv = self.nvml
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            return nv.nvmlDeviceGetHandleByUUID(("GPU-" + uuid).encode())
         except Exception:
-            self.proc = None
+            vis = [v.strip() for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
+                   if v.strip()]
+            idx = int(vis[device_index]) if device_index < len(vis) and vis[device_index].isdigit() \
+                else device_index
+            return nv.nvmlDeviceGetHandleByIndex(idx)
+
+    def _run(self):
+        nv, h = self.nvml, self.handle
+        get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self.stop_ev.is_set():
+            try:
+                t = time.perf_counter()
+                sm = float(nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM))
+                pw = nv.nvmlDeviceGetPowerUsage(h) / 1000.0
+                rs = int(get_reasons(h))
+                self.samples.append((t, sm, pw, rs))
+            except Exception as e:
+                self.err = str(e)
+                self.ready.set()
+                return
+            self.ready.set()
+            time.sleep(0.001)
+
+    def mark_start(self):
+        self.t0 = time.perf_counter()
+
+    def mark_end(self):
+        self.t1 = time.perf_counter()
 
     def stop(self) -> dict:
-        if not self.proc:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
+        if self.nvml is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [self.err or "no nvml"]}
+        self.stop_ev.set()
+        self.thread.join(2.0)
+        t0 = self.t0 if self.t0 is not None else -math.inf
+        t1 = self.t1 if self.t1 is not None else math.inf
+        inside = [x for x in self.samples if t0 <= x[0] <= t1]
+        # a region shorter than the sampling period: take the samples nearest to it
+        if not inside and self.samples:
+            mid = 0.5 * (t0 + t1) if math.isfinite(t0) and math.isfinite(t1) else self.samples[-1][0]
+            inside = sorted(self.samples, key=lambda x: abs(x[0] - mid))[:3]
         try:
-            self.proc.wait(timeout=5)
+            self.nvml.nvmlShutdown()
         except Exception:
-            self.proc.kill()
-        self.out.close()
-        sm, smax, reasons, power = [], [], set(), []
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
-                power.append(float(f[3]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        os.unlink(self.path)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        top = max(power) if power else 0.0
-        loaded = [s for s, p in zip(sm, power) if p >= 0.5 * top] or sm
-        return {"sm_mhz": float(np.median(loaded)), "sm_max_mhz": float(max(smax)),
-                "reasons": sorted(reasons), "samples": len(sm), "power_w_max": top}
+            pass
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz,
+                    "reasons": [self.err or "no samples"]}
+        reasons = sorted({n for _, _, _, rs in inside for n, bit in self.REASONS if rs & bit})
+        return {"sm_mhz": float(np.median([x[1] for x in inside])), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(inside),
+                "power_w_max": float(max(x[2] for x in inside)), "source": "nvml, 1 ms"}
 
 
 # ------------------------------------------------------------------ workload on the device
@@ -274,11 +314,13 @@ def run_ours(args, dist: Dist) -> dict:
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         dist.barrier()
         torch.cuda.synchronize()
+        clocks.mark_start()
         start.record(stream)
         for k in range(args.steps):
             wl.step(stream, ev_attn[k], ev_unm[k])
         end.record(stream)
         torch.cuda.synchronize()
+        clocks.mark_end()
         dist.barrier()
     clk = clocks.stop()
     ms = start.elapsed_time(end) / args.steps

@@ -65,6 +65,9 @@ constexpr int kSegCost = 5;
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kRescaleLog2 = 8.f;  // lazy rescale: O is rescaled when the max grows by > 2^8
 constexpr int kTmemCols = 512;
+// Bits of the workspace error word: a role that gave up on a wait (bit role-1:
+// 1 TMA producer, 2 MMA issuer, 4 softmax warps) and a context length outside [0, Lmax].
+constexpr int kErrCtxLen = 8;
 
 template <int D>
 struct Cfg {
@@ -689,7 +692,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         int local = 0;
         for (int p = p0; p < p1; ++p) {
             int L = a.lens[p / (a.Hkv * a.NRG)];
-            L = L < 0 ? 0 : (L > a.Lmax ? a.Lmax : L);
+            // a length outside [0, Lmax] is recorded in the error word and clamped, so
+            // no read leaves the cache
+            if (L < 0 || L > a.Lmax) {
+                if (blockIdx.x == 0) atomicOr(a.err_word, kErrCtxLen);
+                L = L < 0 ? 0 : a.Lmax;
+            }
             local += (L + kTN - 1) / kTN + 1 + kSegCost;
         }
         int incl = local;
@@ -799,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(kTmemCols)
                      : "memory");
-    if (t == 0 && *sm.err) atomicOr(a.err_word, *sm.err);
+    if (t == 0 && *sm.err) atomicOr(a.err_word, 1 << (*sm.err - 1));
 }
 
 // Combines the partials of every pair whose tiles were split across CTAs:
@@ -1220,7 +1228,7 @@ extern "C" tt_status tt_block_attn_noalloc(const tt_attn_desc *d, const void *q,
     void *base = nullptr;
     if ((st = static_scratch(&base, fn)) != TT_OK) return st;
     AttnWs w = carve(base, g.npairs, static_cast<size_t>(g.P) + g.npairs, d->d);
-    // the error word and arrival counters must start at zero whatever an earlier call left
+    // the error word and the per-pair split table start at zero whatever an earlier call left
     const size_t head = reinterpret_cast<char *>(w.part_ml) - reinterpret_cast<char *>(base);
     st = cuda_status(cudaMemsetAsync(base, 0, head, (cudaStream_t)stream), fn);
     if (st != TT_OK) return st;

@@ -133,8 +133,11 @@ size_t tt_block_attn_workspace_size(const tt_attn_desc *desc);
  * where the keys of sequence b and KV head g = h/(Hq/Hkv) are the prefix rows
  * k_ctx[b,g,0..L_b-1,:] followed by the block rows k_blk[b,0..S-1,g,:] (values
  * alike).  Every block query sees the whole prefix and all S block keys.
- *   ctx_lens  device int32[B], 0 <= L_b <= Lmax (not checked on the host; a
- *             value outside that range is clamped into it by the kernel).
+ *   ctx_lens  device int32[B], 0 <= L_b <= Lmax.  The lengths live on the
+ *             device, so the host cannot check them: a value outside that range
+ *             sets the flag 8 in the workspace error word (tt_block_attn_error); the
+ *             kernel computes that sequence with the length clamped into range
+ *             (no read leaves the cache); the other sequences are unaffected.
  *   lse       device float[B, Hq, S] natural-log log-sum-exp of the scaled
  *             scores, or NULL.
  *   workspace device, >= tt_block_attn_workspace_size(desc) bytes, 256-byte
@@ -152,10 +155,13 @@ tt_status tt_block_attn(const tt_attn_desc *desc, const void *q, const void *k_c
                         size_t workspace_bytes, tt_stream_t stream);
 
 /*
- * Reads the device error flag of an attention workspace into *flag_out (host):
- * 0 = no kernel that used the workspace has given up on a wait since it was
- * zeroed; otherwise the role that timed out first (1 = TMA producer, 2 = MMA
- * issuer, 3 = softmax warps).  Synchronizes `stream`.
+ * Reads the device error word of an attention workspace into *flag_out (host).
+ * It accumulates over every call that used the workspace since it was zeroed:
+ * 0 = nothing to report; otherwise an OR of
+ *   1  the TMA producer gave up on a wait,   2  an MMA issuer gave up on a wait,
+ *   4  the softmax warps gave up on a wait,  8  a ctx_lens value was outside
+ *      [0, Lmax] (that sequence was computed with the length clamped).
+ * A wait that gives up leaves `out` incomplete.  Synchronizes `stream`.
  */
 tt_status tt_block_attn_error(const void *workspace, int32_t *flag_out, tt_stream_t stream);
 
@@ -176,10 +182,14 @@ tt_status tt_block_attn_error(const void *workspace, int32_t *flag_out, tt_strea
  *    SMs the prefix is split across fewer SMs (same result up to fp32 rounding).
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress); make that first call before any stream capture.
- *  - Every call shares the one array and clears its arrival counters on
- *    `stream` before the kernel: calls that overlap on the GPU (other streams,
- *    other host threads without ordering) race and corrupt each other's
- *    results.  Order them on one stream.
+ *  - Every call shares the one array and clears its error word and per-pair
+ *    split table on `stream` before the kernel: calls that overlap on the GPU
+ *    (other streams, other host threads without ordering) race and corrupt each
+ *    other's results.  Order them on one stream.
+ *  - The error word lives in the shared array and is cleared by the next call,
+ *    and no entry point reads it: a kernel wait that gives up or a ctx_lens value
+ *    out of range (see tt_block_attn_error) is NOT reported by this variant.
+ *    Callers that need those reports use tt_block_attn with a workspace.
  */
 tt_status tt_block_attn_noalloc(const tt_attn_desc *desc, const void *q, const void *k_ctx,
                                 const void *v_ctx, const int32_t *ctx_lens, const void *k_blk,

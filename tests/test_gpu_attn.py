@@ -149,3 +149,33 @@ def test_full_size_ragged16k_sampled():
 
 def test_full_size_long_sampled():
     _sampled_full_size("long", lambda lens: [2])
+
+
+def test_out_of_range_lengths_are_reported_and_clamped():
+    """ctx_lens lives on the device, so the host cannot validate it: a length below 0 or
+    above Lmax sets flag 8 of the workspace error word, and that sequence is computed
+    with its length clamped into [0, Lmax].  A call with valid lengths leaves the word 0."""
+    import ctypes
+    shape = synth.AttnShape(3, 16, 8, 2, 128, 200, lens=[0, 77, 200])
+    inp = synth.attn_inputs(shape, seed=31)
+    d = _gpu.attn_dev(inp)
+    desc = tt.attn_desc(d["q"], d["k_ctx"], d["v_ctx"], d["k_blk"], d["v_blk"], d["q"])
+    lib = tt.load()
+
+    def flag(ws):
+        f = ctypes.c_int32(-1)
+        tt.check(lib.tt_block_attn_error(ws.ptr, ctypes.byref(f), None))
+        return f.value
+
+    ws = tt.Workspace(tt.block_attn_workspace_size(desc))
+    ref, _ = oracle.block_attn(inp["q"], inp["k_ctx"], inp["v_ctx"], inp["ctx_lens"],
+                               inp["k_blk"], inp["v_blk"])
+    out = tt.block_attn(d["q"], d["k_ctx"], d["v_ctx"], d["ctx_lens"], d["k_blk"], d["v_blk"],
+                        workspace=ws)
+    torch.cuda.synchronize()
+    assert flag(ws) == 0
+    bad = torch.tensor([-5, 77, 210], dtype=torch.int32, device=_gpu.DEV)
+    out = tt.block_attn(d["q"], d["k_ctx"], d["v_ctx"], bad, d["k_blk"], d["v_blk"], workspace=ws)
+    torch.cuda.synchronize()
+    assert flag(ws) == 8
+    _gpu.assert_attn_close(out.float().cpu().numpy().astype(np.float64), ref, what="clamped")

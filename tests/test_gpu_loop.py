@@ -124,3 +124,52 @@ def test_producer_error_stops_loop():
     torch.cuda.synchronize()
     assert (steps_used.cpu().numpy() == 2).all()  # two finished steps, state consistent
     assert (masked.cpu().numpy().sum(axis=1) == S - 2).all()
+
+
+def test_host_watchdog_reports_timeout_and_state_stays_resumable():
+    """The loop's bounded host wait: a producer whose stream work is held up on the
+    host (a host function that sleeps 300 ms, enqueued through the driver API) makes
+    the per-step wait run out after timeout_ms = 50.  The call returns TT_ERR_TIMEOUT
+    having counted no finished step; once the stream drains, the device state is that
+    of step 0, and a resumed call finishes the block exactly as the oracle does."""
+    import ctypes
+    import time
+
+    B, S, V = 2, 8, 300
+    fn = lambda k: synth.counter_logits(4, k, B, S, V, 0.25, 0.2, "f32")  # noqa: E731
+    cuda = ctypes.CDLL("libcuda.so.1")
+    cuda.cuLaunchHostFunc.restype = ctypes.c_int
+    cuda.cuLaunchHostFunc.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    HOSTFN = ctypes.CFUNCTYPE(None, ctypes.c_void_p)
+    slept = []
+
+    def _sleep(_user):
+        time.sleep(0.3)
+        slept.append(1)
+
+    host_fn = HOSTFN(_sleep)
+    # logits staged on the device first: a copy from pageable host memory would wait
+    # for the stream (and so for the sleeping host function) before the loop's wait
+    staged = [torch.from_numpy(fn(k)).to(_gpu.DEV) for k in range(S)]
+    torch.cuda.synchronize()
+
+    def producer(step, buf):
+        if step == 0:
+            s = torch.cuda.current_stream().cuda_stream
+            assert cuda.cuLaunchHostFunc(ctypes.c_void_p(s), ctypes.cast(host_fn, ctypes.c_void_p),
+                                         None) == 0
+        buf.copy_(staged[step], non_blocking=True)
+
+    tokens, masked, steps_used, cstep = _state(B, S)
+    with pytest.raises(tt.TTError) as e:
+        tt.denoise_block_loop(B, S, V, tt.TT_F32, 0.1, 1.5, 3, S, tokens, masked, steps_used,
+                              cstep, producer=producer, timeout_ms=50)
+    assert e.value.status == tt.TT_ERR_TIMEOUT
+    torch.cuda.synchronize()
+    assert slept == [1]
+    one = oracle.block_loop(B, S, fn, "f32", 0.1, 1.5, 3, S, stop_step=1)
+    _compare(one, tokens, masked, steps_used, cstep)
+    tt.denoise_block_loop(B, S, V, tt.TT_F32, 0.1, 1.5, 3, S, tokens, masked, steps_used, cstep,
+                          producer=producer, start_step=1)
+    torch.cuda.synchronize()
+    _compare(oracle.block_loop(B, S, fn, "f32", 0.1, 1.5, 3, S), tokens, masked, steps_used, cstep)

@@ -6,9 +6,9 @@ synchronisation an allocation can cause -- so they cannot provide the workspace
 tt_block_attn asks for.  This entry point takes no workspace and allocates
 nothing: its scratch is a fixed array inside libtt.  The test calls it through
 the C ABI twice in a row (the second call reuses the scratch the first left
-behind) and checks each output against the workspace entry point's, within the
-attention tolerances the other GPU tests use.  It runs last so that a failure
-here cannot hide the results of the other tests.
+behind) and checks each output against the workspace entry point's, and against
+the fp64 oracle, within the attention tolerances the other GPU tests use.  It runs
+last so that a failure here cannot hide the results of the other tests.
 """
 import ctypes
 
@@ -16,6 +16,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from block_mask_diffusion_tt_b300 import synth, tt
 import _gpu
 
@@ -35,11 +36,18 @@ def _noalloc_raw(d, out, lse):
               d["v_blk"].data_ptr(), out.data_ptr(), lse.data_ptr(), stream)
 
 
+_RNG = np.random.default_rng(120)
+
+
 @pytest.mark.parametrize("shape", [
     synth.AttnShape(4, 16, 32, 2, 128, 3000, lens=[3000, 17, 1500, 0]),
     synth.AttnShape(1, 16, 16, 1, 128, 40000, lens=[40000]),  # one pair over every SM
     synth.AttnShape(3, 16, 8, 2, 64, 700, lens=[700, 64, 300]),
-], ids=["ragged", "long-single", "d64"])
+    # 240 pairs at d=128: the scratch then holds fewer partial slots than the device has
+    # SMs, so the prefix is split over a reduced number of CTAs
+    synth.AttnShape(120, 16, 32, 2, 128, 300,
+                    lens=[int(x) for x in _RNG.integers(0, 301, size=120)]),
+], ids=["ragged", "long-single", "d64", "240-pairs"])
 def test_noalloc_matches_workspace_entry_point_twice(shape):
     for call, seed in enumerate((21, 22)):
         inp = synth.attn_inputs(shape, seed=seed)
@@ -57,6 +65,10 @@ def test_noalloc_matches_workspace_entry_point_twice(shape):
         want = ref.float().cpu().numpy().astype(np.float64)
         _gpu.assert_attn_close(got, want, lse.cpu().numpy(), ref_lse.cpu().numpy(),
                                f"noalloc call {call + 1}")
+        exact, exact_lse = oracle.block_attn(inp["q"], inp["k_ctx"], inp["v_ctx"],
+                                             inp["ctx_lens"], inp["k_blk"], inp["v_blk"])
+        _gpu.assert_attn_close(got, exact, lse.cpu().numpy(), exact_lse,
+                               f"noalloc call {call + 1} against the oracle")
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
