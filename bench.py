@@ -115,6 +115,60 @@ class Dist:
 
 
 # ------------------------------------------------------------------ clocks
+class _CtypesNvml:
+    """The few read-only NVML queries the clock sampler uses, called through ctypes on
+    the driver's libnvidia-ml (for hosts without the nvidia-ml-py module)."""
+    NVML_CLOCK_SM = 1
+
+    def __init__(self):
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+
+    def _ok(self, r, what):
+        if r != 0:
+            raise RuntimeError(f"{what} returned {r}")
+
+    def nvmlInit(self):
+        self._ok(self.lib.nvmlInit_v2(), "nvmlInit_v2")
+
+    def nvmlShutdown(self):
+        self.lib.nvmlShutdown()
+
+    def nvmlDeviceGetHandleByUUID(self, uuid: bytes):
+        h = ctypes.c_void_p()
+        self._ok(self.lib.nvmlDeviceGetHandleByUUID(ctypes.c_char_p(uuid), ctypes.byref(h)),
+                 "nvmlDeviceGetHandleByUUID")
+        return h
+
+    def nvmlDeviceGetHandleByIndex(self, i: int):
+        h = ctypes.c_void_p()
+        self._ok(self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(i), ctypes.byref(h)),
+                 "nvmlDeviceGetHandleByIndex_v2")
+        return h
+
+    def nvmlDeviceGetClockInfo(self, h, clock: int) -> int:
+        v = ctypes.c_uint()
+        self._ok(self.lib.nvmlDeviceGetClockInfo(h, ctypes.c_int(clock), ctypes.byref(v)),
+                 "nvmlDeviceGetClockInfo")
+        return v.value
+
+    def nvmlDeviceGetMaxClockInfo(self, h, clock: int) -> int:
+        v = ctypes.c_uint()
+        self._ok(self.lib.nvmlDeviceGetMaxClockInfo(h, ctypes.c_int(clock), ctypes.byref(v)),
+                 "nvmlDeviceGetMaxClockInfo")
+        return v.value
+
+    def nvmlDeviceGetPowerUsage(self, h) -> int:
+        v = ctypes.c_uint()
+        self._ok(self.lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(v)), "nvmlDeviceGetPowerUsage")
+        return v.value
+
+    def nvmlDeviceGetCurrentClocksThrottleReasons(self, h) -> int:
+        v = ctypes.c_ulonglong()
+        self._ok(self.lib.nvmlDeviceGetCurrentClocksThrottleReasons(h, ctypes.byref(v)),
+                 "nvmlDeviceGetCurrentClocksThrottleReasons")
+        return v.value
+
+
 class ClockSampler:
     """Samples the GPU's SM clock, power and clock-event reasons during the timed region.
 
@@ -134,7 +188,10 @@ class ClockSampler:
         self.ready = threading.Event()
         self.max_mhz = None
         try:
-            import pynvml
+            try:
+                import pynvml
+            except ImportError:  # the driver's libnvidia-ml through ctypes
+                pynvml = _CtypesNvml()
             pynvml.nvmlInit()
             self.nvml = pynvml
             self.handle = self._handle(device_index)

@@ -18,6 +18,24 @@ int sm_count();
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// A logits producer of the in-block loop: a function and its context.
+struct LoopProducer {
+    tt_status (*fn)(void *ctx, int32_t step, const int32_t *tokens, const uint8_t *is_masked,
+                    void *logits, tt_stream_t stream);
+    void *ctx;
+};
+// The in-block iteration (unmask.cu): tt_denoise_block_loop's steps; with
+// init_active (device uint8[B], nullable) a start at step 0 masks only the
+// positions of the sequences that take part.
+tt_status run_block_loop(const tt_unmask_desc *d, int32_t steps_per_block, int32_t start_step,
+                         int32_t stop_step, const LoopProducer &prod, void *logits_buf,
+                         int32_t *tokens, uint8_t *is_masked, int32_t *steps_used,
+                         int32_t *committed_step, const uint8_t *init_active, void *workspace,
+                         size_t workspace_bytes, cudaStream_t stream, int32_t timeout_ms,
+                         int32_t *steps_run, const char *fn);
+// Bytes of the workspace run_block_loop needs (0 on an invalid desc).
+size_t block_loop_workspace_bytes(const tt_unmask_desc *d);
+
 // Simple bump allocator over a caller-provided workspace.
 struct Carve {
     char *base;
@@ -56,6 +74,26 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
+// Packed fp32 pairs (sm_100 f32x2 instructions).
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void upk2(uint64_t r, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // ---------------------------------------------------------------- mbarriers
 // Every wait on an mbarrier is bounded: after kWaitLimitNs it records an error code
 // and returns false, so a kernel that would otherwise wait forever stops instead.
@@ -80,6 +118,19 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
         "selp.u32 %0, 1, 0, p;\n\t}\n"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// try_wait that may suspend the thread until the phase completes (or hint_ns
+// passes), so a waiting warp takes no issue slots from the warps doing work.
+__device__ __forceinline__ bool mbar_try_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
         : "memory");
     return ok != 0;
 }
@@ -142,6 +193,54 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
                 }
             }
             if (__shfl_sync(0xFFFFFFFFu, stop, 0)) return false;
+        }
+    }
+}
+// Warp-collective wait that sleeps between polls (__nanosleep, backing off from 32
+// to 256 ns, then a try_wait that may suspend): for warps that wait most of the
+// time, where spinning would take issue slots from the warps doing the work.  Same
+// bounds and error flag as warp_wait.
+__device__ __forceinline__ bool warp_wait_sleep(uint32_t bar, uint32_t parity, volatile int *err,
+                                                int code) {
+    if (__any_sync(0xFFFFFFFFu, mbar_try(bar, parity))) return true;
+    uint64_t t0 = 0;
+    uint32_t nap = 32;
+    for (uint32_t i = 1;; ++i) {
+        __nanosleep(nap);
+        if (nap < 256) nap <<= 1;
+        if (__any_sync(0xFFFFFFFFu, mbar_try_sleep(bar, parity, 20000u))) return true;
+        if ((i & 15) == 0) {
+            int stop = 0;
+            if ((threadIdx.x & 31) == 0) {
+                const uint64_t now = globaltimer();
+                if (t0 == 0) t0 = now;
+                if (*err) {
+                    stop = 1;
+                } else if (now - t0 > kWaitLimitNs) {
+                    atomicCAS(const_cast<int *>(err), 0, code);
+                    stop = 1;
+                }
+            }
+            if (__shfl_sync(0xFFFFFFFFu, stop, 0)) return false;
+        }
+    }
+}
+// Thread-level form of warp_wait_sleep.
+static __device__ __noinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity,
+                                                    volatile int *err, int code) {
+    if (mbar_try(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    uint32_t nap = 32;
+    for (uint32_t i = 1;; ++i) {
+        __nanosleep(nap);
+        if (nap < 256) nap <<= 1;
+        if (mbar_try_sleep(bar, parity, 20000u)) return true;
+        if ((i & 15) == 0) {
+            if (*err) return false;
+            if (globaltimer() - t0 > kWaitLimitNs) {
+                atomicCAS(const_cast<int *>(err), 0, code);
+                return false;
+            }
         }
     }
 }

@@ -84,6 +84,7 @@ def load(path: str = LIB_PATH):
         "tt_confidence_unmask_workspace_size": (_sz, [ctypes.POINTER(UnmaskDesc)]),
         "tt_confidence_unmask": (ctypes.c_int, [ctypes.POINTER(UnmaskDesc), _p, _p, _p, _p, _p, _p,
                                                 _i32, _p, _sz, _p]),
+        "tt_confidence_unmask_error": (ctypes.c_int, [_p, ctypes.POINTER(_i32), _p]),
         "tt_block_init": (ctypes.c_int, [ctypes.POINTER(UnmaskDesc), _p, _p, _p, _p, _p]),
         "tt_denoise_block_loop_workspace_size": (_sz, [ctypes.POINTER(UnmaskDesc)]),
         "tt_denoise_block_loop": (ctypes.c_int, [ctypes.POINTER(UnmaskDesc), _i32, _i32, _i32, _p,
@@ -396,6 +397,6 @@ def exported_symbols() -> list:
             "tt_block_attn_workspace_size", "tt_block_attn", "tt_block_attn_error",
             "tt_block_attn_noalloc",
             "tt_confidence_unmask_workspace_size",
-            "tt_confidence_unmask", "tt_block_init", "tt_denoise_block_loop_workspace_size",
+            "tt_confidence_unmask", "tt_confidence_unmask_error", "tt_block_init", "tt_denoise_block_loop_workspace_size",
             "tt_denoise_block_loop",
             "tt_synth_logits", "tt_synth_logits_producer", "tt_kv_append"]

@@ -45,10 +45,10 @@
  *    are validated on the host before any launch; on TT_ERR_INVALID_ARG,
  *    TT_ERR_UNSUPPORTED or TT_ERR_WORKSPACE nothing was enqueued.
  *    tt_last_error() gives a message for the calling thread's last failure.
- *  - Workspaces hold arrival counters that must be zero before a workspace's
- *    first use: zero it once (tt_workspace_zero or any memset) after allocating
- *    it.  Every successful call leaves the counters at zero again.  Calls that
- *    share a workspace must be ordered on one stream.
+ *  - A workspace starts with an error word that must be zero before the
+ *    workspace's first use: zero the workspace once (tt_workspace_zero or any
+ *    memset) after allocating it.  The kernels keep no other state in it between
+ *    calls.  Calls that share a workspace must be ordered on one stream.
  *  - bf16 is IEEE bfloat16 bit patterns (uint16).  Strides are in elements.
  */
 #ifndef TT_H_
@@ -241,6 +241,17 @@ tt_status tt_confidence_unmask(const tt_unmask_desc *desc, const void *logits, i
                                uint8_t *is_masked, float *conf, uint8_t *committed_now,
                                int32_t *remaining, int32_t force_commit_all, void *workspace,
                                size_t workspace_bytes, tt_stream_t stream);
+
+/*
+ * Reads the error word of an unmask (or block-loop) workspace into *flag_out
+ * (host): 0 = nothing to report since the workspace was zeroed; otherwise an OR
+ * of 1 (the kernel's copy-issuing thread gave up on a wait) and 2 (its reducing
+ * warps gave up on a wait).  A wait that gives up leaves that step's outputs
+ * incomplete; tt_denoise_block_loop checks the word after every step and returns
+ * TT_ERR_INTERNAL when it is set.  Synchronizes `stream`.
+ */
+tt_status tt_confidence_unmask_error(const void *workspace, int32_t *flag_out,
+                                     tt_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* In-block loop                                                             */

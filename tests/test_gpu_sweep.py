@@ -76,7 +76,9 @@ def test_unmask_s64_partial_state_and_fallback():
     position commits per sequence."""
     B, S, V = 8, 64, 131072
     rng = np.random.default_rng(64)
-    logits = synth.counter_logits(3, 1, B, S, V, W.sigma, 0.5, "bf16")
+    # no spikes: with spikes several rows reach confidences just below 1.0f, and the
+    # fallback between them is too close to call in fp32 (the oracle flags it)
+    logits = synth.counter_logits(3, 1, B, S, V, W.sigma, 0.0, "bf16")
     masked = (rng.random((B, S)) < 0.3).astype(np.uint8)
     masked[:, 63] = 1  # the last position of every sequence is masked
     masked[5] = 0
