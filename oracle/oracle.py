@@ -128,7 +128,8 @@ def confidence_unmask(logits, dtype: str, temperature: float, threshold: float,
 def block_loop(B: int, S: int, logits_fn: Callable[[int], np.ndarray], dtype: str,
                temperature: float, threshold: float, mask_token_id: int, steps_per_block: int,
                start_step: int = 0, state: Optional[dict] = None,
-               stop_step: Optional[int] = None, nthreads: int = 0, lib=None) -> dict:
+               stop_step: Optional[int] = None, nthreads: int = 0, lib=None,
+               active: Optional[np.ndarray] = None) -> dict:
     """In-block iteration of the denoiser step.
 
     A block starts as S copies of mask_token_id, all masked.  For step k in
@@ -138,13 +139,17 @@ def block_loop(B: int, S: int, logits_fn: Callable[[int], np.ndarray], dtype: st
     forward), run one unmask step -- forcing every remaining position to commit
     at the last step -- and count the step for each sequence that still had a
     masked position.  ``state`` (tokens, is_masked, steps_used, committed_step)
-    resumes an interrupted loop.  Follows the block-by-block mechanism of the
-    dothoosh.com article (section "two-tower mechanism") and the generate
-    arguments of the 889990.xyz code example.
+    resumes an interrupted loop.  ``active`` (bool/uint8 [B]) restricts a fresh
+    block to the sequences that take part: the others start with nothing masked.
+    Follows the block-by-block mechanism of the dothoosh.com article (section
+    "two-tower mechanism") and the generate arguments of the 889990.xyz code
+    example.
     """
     if state is None or start_step == 0:
         tokens = np.full((B, S), mask_token_id, dtype=np.int32)
         masked = np.ones((B, S), dtype=np.uint8)
+        if active is not None:
+            masked[np.asarray(active).reshape(B) == 0] = 0
         steps_used = np.zeros((B,), dtype=np.int32)
         committed_step = np.full((B, S), -1, dtype=np.int32)
     else:
@@ -206,3 +211,82 @@ def kv_append(k_ctx: list, v_ctx: list, ctx_lens, k_blk: list, v_blk: list,
                     out_v[layer][b, g, L + s, :] = v_blk[layer][b, s, g, :]
         new_lens[b] = L + S
     return dict(k_ctx=out_k, v_ctx=out_v, ctx_lens=new_lens, overflow=overflow)
+
+
+def generate_blocks(B: int, S: int, logits_fn: Callable[[int, int], np.ndarray],
+                    kv_fn: Callable[[int, np.ndarray], tuple], k_ctx: list, v_ctx: list,
+                    ctx_lens, dtype: str, temperature: float, threshold: float,
+                    mask_token_id: int, steps_per_block: int, max_new_tokens: int,
+                    eos_token_id: int = -1, active=None, out_fill: int = -1) -> dict:
+    """Block-by-block generation: blocks of S positions are denoised one after another,
+    and each finished block becomes context for the next.
+
+    The pages describe this outer loop: the denoiser fills a block of masked
+    positions step by step, the clean block is handed to the context tower, and the
+    next block attends to the longer prefix (dothoosh.com, "فرآیند انتشار در برابر
+    رمزگشایی متوالی در مدل جدید انویدیا", section on the two-tower mechanism); the
+    generate call takes max_new_tokens, block_size, steps_per_block and
+    eos_token_id (889990.xyz, "NVIDIA发布Nemotron两塔模型", section 训练与推理, code
+    example).  Readings, where the pages are silent:
+
+    * the number of blocks is ceil(max_new_tokens / S); positions of the last block
+      past max_new_tokens are generated but not kept;
+    * a sequence stops after the block in which it commits eos_token_id; its
+      generated length counts the tokens up to and including the first EOS of the
+      kept positions; a sequence also stops at max_new_tokens, and when its context
+      cache cannot take another block (counted in ``overflow``);
+    * a stopped sequence takes no part in later blocks (nothing masked, nothing
+      appended); only sequences that continue get the block's K/V appended, and
+      after the last block nothing is appended.
+
+    logits_fn(block, step) gives [B,S,V] logits (the denoiser forward's stand-in);
+    kv_fn(block, tokens [B,S]) gives (k list, v list) per layer [B,S,Hkv,d] for the
+    committed block (the context tower's stand-in).  Returns out_tokens [B,
+    max_new_tokens] (``out_fill`` where nothing was generated), gen_len [B], the
+    final active flags, context lengths and caches, steps_total [B], blocks_run and
+    overflow.
+    """
+    n_blocks = -(-max_new_tokens // S)
+    act = np.ones(B, dtype=np.uint8) if active is None else np.array(active, np.uint8, copy=True)
+    out = np.full((B, max_new_tokens), out_fill, dtype=np.int32)
+    gen_len = np.zeros(B, dtype=np.int32)
+    steps_total = np.zeros(B, dtype=np.int32)
+    lens = np.array(ctx_lens, dtype=np.int32, copy=True)
+    kc = [np.array(k, copy=True) for k in k_ctx]
+    vc = [np.array(v, copy=True) for v in v_ctx]
+    Lmax = kc[0].shape[2]
+    overflow = 0
+    blocks_run = 0
+    ambiguous = 0
+    for blk in range(n_blocks):
+        if not act.any():
+            break
+        r = block_loop(B, S, lambda k: logits_fn(blk, k), dtype, temperature, threshold,
+                       mask_token_id, steps_per_block, active=act)
+        ambiguous += r["ambiguous"]
+        blocks_run += 1
+        keep = min(S, max_new_tokens - blk * S)
+        for b in range(B):
+            if not act[b]:
+                continue
+            toks = r["tokens"][b, :keep]
+            out[b, blk * S: blk * S + keep] = toks
+            steps_total[b] += r["steps_used"][b]
+            hits = np.nonzero(toks == eos_token_id)[0] if eos_token_id >= 0 else []
+            if len(hits):
+                gen_len[b] = blk * S + int(hits[0]) + 1
+                act[b] = 0
+                continue
+            gen_len[b] = blk * S + keep
+            if gen_len[b] == max_new_tokens:
+                act[b] = 0
+            elif lens[b] + S > Lmax:  # the cache cannot take this block
+                act[b] = 0
+                overflow += 1
+        if blk + 1 < n_blocks and act.any():
+            kb, vb = kv_fn(blk, r["tokens"])
+            a = kv_append(kc, vc, lens, kb, vb, active=act)
+            kc, vc, lens = a["k_ctx"], a["v_ctx"], a["ctx_lens"]
+    return dict(out_tokens=out, gen_len=gen_len, active=act, ctx_lens=lens, k_ctx=kc, v_ctx=vc,
+                steps_total=steps_total, blocks_run=blocks_run, overflow=overflow,
+                ambiguous=ambiguous)
