@@ -60,6 +60,13 @@ class KvDesc(ctypes.Structure):
 
 
 LOGITS_FN = ctypes.CFUNCTYPE(ctypes.c_int, _p, _i32, _p, _p, _p, _p)
+BLOCK_LOGITS_FN = ctypes.CFUNCTYPE(ctypes.c_int, _p, _i32, _i32, _p, _p, _p, _p)
+BLOCK_KV_FN = ctypes.CFUNCTYPE(ctypes.c_int, _p, _i32, _p, _p, _p, _p, _p)
+
+
+class GenerateParams(ctypes.Structure):
+    _fields_ = [("max_new_tokens", _i32), ("eos_token_id", _i32), ("steps_per_block", _i32),
+                ("timeout_ms", _i32)]
 
 _lib = None
 
@@ -94,6 +101,11 @@ def load(path: str = LIB_PATH):
                                            ctypes.c_float, ctypes.c_uint64, _p, _p]),
         "tt_synth_logits_producer": (ctypes.c_int, [_p, _i32, _p, _p, _p, _p]),
         "tt_kv_append": (ctypes.c_int, [ctypes.POINTER(KvDesc), _p, _p, _p, _p, _p, _p, _p, _p]),
+        "tt_generate_blocks_workspace_size": (_sz, [ctypes.POINTER(UnmaskDesc)]),
+        "tt_generate_blocks": (ctypes.c_int, [ctypes.POINTER(UnmaskDesc), ctypes.POINTER(KvDesc),
+                                              ctypes.POINTER(GenerateParams), _p, _p, _p, _p,
+                                              _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p,
+                                              _sz, _p, ctypes.POINTER(_i32)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -391,6 +403,84 @@ def kv_append(k_ctx: list, v_ctx: list, ctx_lens, k_blk: list, v_blk: list, acti
                               ptrs[3], _ptr(active), _ptr(overflow), _stream(stream)))
 
 
+# ------------------------------------------------------------------ block-by-block generation
+def _kv_desc(k_ctx: list, k_blk: list) -> KvDesc:
+    B, Hkv, Lmax, d = k_ctx[0].shape
+    desc = KvDesc(B=B, S=k_blk[0].shape[1], Hkv=Hkv, d=d, Lmax=Lmax, n_layers=len(k_ctx))
+    desc.ctx_strides = _i64x4(*k_ctx[0].stride())
+    desc.blk_strides = _i64x4(*k_blk[0].stride())
+    return desc
+
+
+def generate_blocks(logits_fn: Callable, kv_fn: Callable, V: int, logits_dtype: int,
+                    temperature: float, threshold: float, mask_token_id: int,
+                    steps_per_block: int, max_new_tokens: int, eos_token_id: int,
+                    k_ctx: list, v_ctx: list, ctx_lens, k_blk: list, v_blk: list,
+                    out_tokens, gen_len, active, steps_total=None, overflow=None,
+                    timeout_ms: int = 60000, stream=None) -> int:
+    """Block-by-block generation (tt_generate_blocks); returns the number of blocks run.
+
+    logits_fn(block, step, logits_buf) fills the [B,S,V] logits on the current
+    stream; kv_fn(block, tokens, active, k_blk, v_blk) fills the per-layer block
+    K/V tensors.  out_tokens int32[B,max_new], gen_len int32[B], active uint8[B]
+    (in/out), steps_total int32[B] and overflow int32[1] (optional) are device
+    tensors updated in place; the caches and ctx_lens as for kv_append.
+    """
+    lib = load()
+    B, S = k_blk[0].shape[0], k_blk[0].shape[1]
+    dt = torch.bfloat16 if logits_dtype == TT_BF16 else torch.float32
+    logits_buf = torch.empty((B, S, V), dtype=dt, device="cuda")
+    desc = unmask_desc(B, S, V, logits_dtype, temperature, threshold, mask_token_id)
+    kdesc = _kv_desc(k_ctx, k_blk)
+    params = GenerateParams(max_new_tokens=max_new_tokens, eos_token_id=eos_token_id,
+                            steps_per_block=steps_per_block, timeout_ms=timeout_ms)
+    ws = Workspace(int(lib.tt_generate_blocks_workspace_size(ctypes.byref(desc))))
+
+    def _logits(_user, block, step, _tok, _msk, _out, _stream):
+        try:
+            logits_fn(int(block), int(step), logits_buf)
+            return TT_OK
+        except Exception:  # reported as TT_ERR_CALLBACK
+            return TT_ERR_INTERNAL
+
+    tokens_view = {}
+
+    def _kv(_user, block, tok_ptr, act_ptr, _kb, _vb, _stream):
+        try:
+            if "t" not in tokens_view:
+                # the library's block tokens [B, S] (device), wrapped without a copy
+                tokens_view["t"] = _device_int32(tok_ptr, (B, S))
+            kv_fn(int(block), tokens_view["t"], active, k_blk, v_blk)
+            return TT_OK
+        except Exception:
+            return TT_ERR_INTERNAL
+
+    cb_l, cb_k = BLOCK_LOGITS_FN(_logits), BLOCK_KV_FN(_kv)
+    arr = ctypes.c_void_p * len(k_ctx)
+    ptrs = [arr(*[t.data_ptr() for t in lst]) for lst in (k_ctx, v_ctx, k_blk, v_blk)]
+    blocks = _i32(0)
+    status = lib.tt_generate_blocks(ctypes.byref(desc), ctypes.byref(kdesc), ctypes.byref(params),
+                                    ctypes.cast(cb_l, _p), None, ctypes.cast(cb_k, _p), None,
+                                    _ptr(logits_buf), ptrs[0], ptrs[1], _ptr(ctx_lens), ptrs[2],
+                                    ptrs[3], _ptr(out_tokens), _ptr(gen_len), _ptr(active),
+                                    _ptr(steps_total), _ptr(overflow), ws.ptr, ws.nbytes,
+                                    _stream(stream), ctypes.byref(blocks))
+    check(status)
+    return int(blocks.value)
+
+
+def _device_int32(ptr, shape):
+    """A torch int32 tensor over device memory owned by the library (no copy)."""
+    n = 1
+    for x in shape:
+        n *= x
+
+    class _Cuda:
+        __cuda_array_interface__ = {"shape": tuple(shape), "typestr": "<i4",
+                                    "data": (int(ptr), False), "version": 3, "strides": None}
+    return torch.as_tensor(_Cuda(), device="cuda")
+
+
 def exported_symbols() -> list:
     """Names of the entry points this binding expects libtt.so to export."""
     return ["tt_status_string", "tt_last_error", "tt_abi_version", "tt_workspace_zero",
@@ -399,4 +489,5 @@ def exported_symbols() -> list:
             "tt_confidence_unmask_workspace_size",
             "tt_confidence_unmask", "tt_confidence_unmask_error", "tt_block_init", "tt_denoise_block_loop_workspace_size",
             "tt_denoise_block_loop",
-            "tt_synth_logits", "tt_synth_logits_producer", "tt_kv_append"]
+            "tt_synth_logits", "tt_synth_logits_producer", "tt_kv_append",
+            "tt_generate_blocks_workspace_size", "tt_generate_blocks"]

@@ -382,6 +382,78 @@ tt_status tt_kv_append(const tt_kv_desc *desc, void *const *k_ctx, void *const *
                        int32_t *ctx_lens, const void *const *k_blk, const void *const *v_blk,
                        const uint8_t *active, int32_t *overflow, tt_stream_t stream);
 
+/* ------------------------------------------------------- block-by-block generation
+ *
+ * Blocks of S positions are generated one after another: each block is denoised by
+ * the in-block loop, its tokens are kept, and -- unless generation ends -- the
+ * committed block's K/V (from the caller's context-tower stand-in) joins every
+ * layer's context cache, so the next block attends to a prefix S tokens longer
+ * (dothoosh.com, "فرآیند انتشار در برابر رمزگشایی متوالی در مدل جدید انویدیا",
+ * section "two-tower mechanism"; 889990.xyz, "NVIDIA发布Nemotron两塔模型",
+ * section 训练与推理, code example: max_new_tokens, block_size, steps_per_block,
+ * eos_token_id).
+ */
+
+/* Producer of one step's logits for block `block` (the denoiser forward, or a
+ * stand-in): as tt_logits_fn, with the block index. */
+typedef tt_status (*tt_block_logits_fn)(void *user, int32_t block, int32_t step,
+                                        const int32_t *tokens, const uint8_t *is_masked,
+                                        void *logits_out, tt_stream_t stream);
+
+/* Producer of a committed block's K/V (the context tower's forward over the
+ * block's tokens, or a stand-in): must enqueue on `stream` work that writes, for
+ * every layer l of the K/V desc, k_blk[l] and v_blk[l] ([B, S, Hkv, d] bf16, the
+ * desc's block strides) from tokens [B, S] (device).  Only sequences with
+ * active[b] != 0 (device) are appended; the others' rows may hold anything.  A
+ * non-OK return stops generation with TT_ERR_CALLBACK. */
+typedef tt_status (*tt_block_kv_fn)(void *user, int32_t block, const int32_t *tokens,
+                                    const uint8_t *active, void *const *k_blk,
+                                    void *const *v_blk, tt_stream_t stream);
+
+typedef struct {
+    int32_t max_new_tokens;  /* >= 1; blocks = ceil(max_new_tokens / S) */
+    int32_t eos_token_id;    /* < 0: no end-of-sequence token */
+    int32_t steps_per_block; /* >= 1 */
+    int32_t timeout_ms;      /* bound of each host wait; <= 0 means 60000 */
+} tt_generate_params;
+
+/* Bytes of device workspace tt_generate_blocks needs (0 on invalid desc). */
+size_t tt_generate_blocks_workspace_size(const tt_unmask_desc *desc);
+
+/*
+ * Runs blocks k = 0, 1, ... while some sequence is generating (active[b] != 0),
+ * at most ceil(max_new_tokens / S) of them.  For block k:
+ *   1. the in-block loop (tt_denoise_block_loop's steps, logits from
+ *      logits_fn(user, k, step, ...) into logits_buf) over a block that starts
+ *      masked for the generating sequences only;
+ *   2. for every sequence generating at the start of block k, with
+ *      keep = min(S, max_new_tokens - k*S): out_tokens[b, k*S + s] = token s for
+ *      s < keep; if one of those is eos_token_id, gen_len[b] = k*S + (first EOS
+ *      position) + 1 and the sequence stops; otherwise gen_len[b] = k*S + keep,
+ *      and the sequence stops at max_new_tokens, or when another block follows and
+ *      its cache cannot take this one (ctx_lens[b] + S > Lmax; counted in
+ *      *overflow); steps_total[b] grows by the steps the block took;
+ *   3. if another block follows and some sequence still generates:
+ *      kv_fn(kv_user, k, tokens, active, k_blk, v_blk) and tt_kv_append of this
+ *      block for the sequences still generating (ctx_lens grows by S).
+ * Arrays: out_tokens int32[B, max_new_tokens] (positions not generated are not
+ * written), gen_len int32[B] (written for generating sequences), active uint8[B]
+ * in/out, steps_total int32[B] (nullable, accumulated), overflow int32 (nullable,
+ * accumulated) -- all device.  k_ctx, v_ctx, ctx_lens, k_blk, v_blk and `kv` as
+ * for tt_kv_append (kv->B, kv->S equal desc->B, desc->S).  The host waits once per
+ * step (the loop) and once per block, each bounded by timeout_ms.  blocks_run
+ * (host, nullable) receives the number of blocks run.  A producer error returns
+ * TT_ERR_CALLBACK with the blocks before it complete.
+ */
+tt_status tt_generate_blocks(const tt_unmask_desc *desc, const tt_kv_desc *kv,
+                             const tt_generate_params *params, tt_block_logits_fn logits_fn,
+                             void *logits_user, tt_block_kv_fn kv_fn, void *kv_user,
+                             void *logits_buf, void *const *k_ctx, void *const *v_ctx,
+                             int32_t *ctx_lens, void *const *k_blk, void *const *v_blk,
+                             int32_t *out_tokens, int32_t *gen_len, uint8_t *active,
+                             int32_t *steps_total, int32_t *overflow, void *workspace,
+                             size_t workspace_bytes, tt_stream_t stream, int32_t *blocks_run);
+
 #ifdef __cplusplus
 }
 #endif
