@@ -290,3 +290,30 @@ def generate_blocks(B: int, S: int, logits_fn: Callable[[int, int], np.ndarray],
     return dict(out_tokens=out, gen_len=gen_len, active=act, ctx_lens=lens, k_ctx=kc, v_ctx=vc,
                 steps_total=steps_total, blocks_run=blocks_run, overflow=overflow,
                 ambiguous=ambiguous)
+
+
+def mamba_state_seed(src: list, dst: list, active=None) -> list:
+    """Seeds the denoiser's Mamba-2 layers with the context tower's states.
+
+    The pages describe the coupling: the denoiser's Mamba-2 layers take their initial
+    state directly from the corresponding Mamba layer of the context tower
+    (dothoosh.com, "فرآیند انتشار در برابر رمزگشایی متوالی در مدل جدید انویدیا",
+    architecture bullets), that is, the context tower's conv/SSM boundary states are
+    injected as the initial states of the denoiser's Mamba layers (aitrends.kr,
+    "Nemotron-Labs-TwoTower-30B-A3B-Base-BF16", section 기술적 특징).  No recurrence
+    is given, so this is the seeding itself: for every layer l, state part p (conv,
+    SSM, ...) and sequence b taking part (``active`` None or active[b] != 0),
+    dst[l][p][b] = src[l][p][b], bytes unchanged; other sequences keep their state.
+
+    src, dst: lists over layers of lists over parts of arrays [B, ...] (any dtype).
+    Returns the new destination arrays.
+    """
+    out = [[np.array(x, copy=True) for x in layer] for layer in dst]
+    for layer in range(len(src)):
+        for part in range(len(src[layer])):
+            B = src[layer][part].shape[0]
+            for b in range(B):
+                if active is not None and not active[b]:
+                    continue
+                out[layer][part][b] = src[layer][part][b]
+    return out
