@@ -11,7 +11,9 @@ device footprint of one layer (a few hundred MB) rather than the whole step.
 over the sweep configuration's block sizes and thresholds (steps = S), and reports
 committed tokens/s and the steps used per block;
 `kvappend` runs `tt_kv_append` for every attention layer of the workload (a
-committed block of S rows joins each layer's context cache).
+committed block of S rows joins each layer's context cache);
+`seed` runs `tt_mamba_state_seed` over 23 Mamba-2 layers for the workload's batch;
+`generate` runs `tt_generate_blocks` for n blocks of the workload.
 
 With --time it instead times back-to-back calls with CUDA events and prints the
 mean time per call and the algorithmic bandwidth.  The timed calls go to the C ABI
@@ -217,9 +219,98 @@ def run_kvappend(w: synth.Workload, n: int, time_it: bool = False):
     return us, nbytes / us / 1e3, f"{L} layers, {n} calls in one CUDA graph"
 
 
+# Mamba-2 layer shapes used for the seeding measurement: 23 layers (the pages' count);
+# per layer and sequence a conv state of 6144 channels x 3 taps in bf16 and an SSM
+# state of 64 heads x 64 x 128 in fp32 (a Mamba-2 layer with 64 heads of 64, state
+# size 128, 8 groups, conv width 4 -- the pages give no layer dimensions).
+SEED_LAYERS = 23
+SEED_CONV = (6144, 3)
+SEED_SSM = (64, 64, 128)
+
+
+def run_seed(w: synth.Workload, n: int, time_it: bool = False):
+    """tt_mamba_state_seed of every Mamba-2 layer for the workload's batch; with time_it,
+    n calls captured in a CUDA graph and the replay timed (bytes read + written)."""
+    B = w.attn.B
+    src = [[torch.randn((B,) + SEED_CONV, device="cuda").to(torch.bfloat16),
+            torch.randn((B,) + SEED_SSM, device="cuda")] for _ in range(SEED_LAYERS)]
+    dst = [[torch.empty_like(a) for a in layer] for layer in src]
+    if not time_it:
+        for _ in range(n):
+            tt.mamba_state_seed(src, dst)
+        return None
+    tt.mamba_state_seed(src, dst)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(n):
+            tt.mamba_state_seed(src, dst)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / n
+    per_seq = sum(a[0].numel() * a.element_size() for a in src[0])
+    nbytes = 2 * SEED_LAYERS * B * per_seq
+    return us, nbytes / us / 1e3, f"{SEED_LAYERS} layers, {n} calls in one CUDA graph"
+
+
+def run_generate(w: synth.Workload, n: int, time_it: bool = False):
+    """tt_generate_blocks on the workload's batch: n blocks of S positions, logits from
+    the counter generator per (block, step), synthetic K/V appended to the workload's
+    attention layers; with time_it, generated tokens per second over the whole call."""
+    a = w.attn
+    g = torch.Generator(device="cuda")
+    g.manual_seed(w.seed)
+    L = w.n_layers
+    Lmax = a.Lmax + n * a.S
+    kc = [torch.randn((a.B, a.Hkv, Lmax, a.d), generator=g, device="cuda").to(torch.bfloat16)
+          for _ in range(L)]
+    vc = [torch.randn((a.B, a.Hkv, Lmax, a.d), generator=g, device="cuda").to(torch.bfloat16)
+          for _ in range(L)]
+    kb = [torch.empty((a.B, a.S, a.Hkv, a.d), dtype=torch.bfloat16, device="cuda")
+          for _ in range(L)]
+    vb = [torch.empty_like(x) for x in kb]
+    lens = torch.from_numpy(synth.ctx_lens_for(a, w.seed)).cuda()
+    thr = synth.spike_threshold(w.spike_p)
+
+    def logits_fn(block, step, buf):
+        tt.synth_logits(w.seed + block, step, a.B, a.S, w.V, w.sigma, thr, tt.TT_BF16, out=buf)
+
+    def kv_fn(block, tokens, active, k_blk, v_blk):
+        for layer in range(L):
+            tt.synth_logits(1000 + block * L + layer, 0, a.B, a.S, a.Hkv * a.d, 1.0, 0,
+                            tt.TT_BF16, out=k_blk[layer].view(a.B, a.S, a.Hkv * a.d))
+            tt.synth_logits(2000 + block * L + layer, 0, a.B, a.S, a.Hkv * a.d, 1.0, 0,
+                            tt.TT_BF16, out=v_blk[layer].view(a.B, a.S, a.Hkv * a.d))
+
+    max_new = n * a.S
+    out = torch.empty((a.B, max_new), dtype=torch.int32, device="cuda")
+    gen_len = torch.zeros((a.B,), dtype=torch.int32, device="cuda")
+    active = torch.ones((a.B,), dtype=torch.uint8, device="cuda")
+    steps = torch.zeros((a.B,), dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    blocks = tt.generate_blocks(logits_fn, kv_fn, w.V, tt.TT_BF16, w.temperature, w.threshold,
+                                w.mask_token_id, w.steps_per_block, max_new, -1, kc, vc, lens,
+                                kb, vb, out, gen_len, active, steps)
+    e1.record()
+    torch.cuda.synchronize()
+    if not time_it:
+        return None
+    us = e0.elapsed_time(e1) * 1e3
+    toks = int(gen_len.sum())
+    mean_steps = float(steps.float().mean()) / max(blocks, 1)
+    return (f"{blocks} blocks, {toks} tokens in {us / 1e3:.2f} ms: {toks / us * 1e6:.0f} "
+            f"generated tokens/s, {mean_steps:.2f} steps per block", None, None)
+
+
 def main():
     ap = argparse.ArgumentParser(description="run one op of the step n times")
-    ap.add_argument("op", choices=["attn", "unmask", "loop", "kvappend"])
+    ap.add_argument("op", choices=["attn", "unmask", "loop", "kvappend", "seed", "generate"])
     ap.add_argument("workload", choices=sorted(synth.workloads()))
     ap.add_argument("n", type=int, nargs="?", default=4)
     ap.add_argument("--time", action="store_true",
@@ -227,13 +318,14 @@ def main():
     args = ap.parse_args()
     tt.load()
     w = synth.workloads()[args.workload]
-    run = dict(attn=run_attn, unmask=run_unmask, loop=run_loop, kvappend=run_kvappend)[args.op]
+    run = dict(attn=run_attn, unmask=run_unmask, loop=run_loop, kvappend=run_kvappend,
+               seed=run_seed, generate=run_generate)[args.op]
     res = run(w, args.n, args.time)
     torch.cuda.synchronize()
     if res is None:
         print("ok", args.op, w.name, args.n)
-    elif args.op == "loop":
-        print(f"loop {w.name}:\n{res[0]}")
+    elif args.op in ("loop", "generate"):
+        print(f"{args.op} {w.name}:\n{res[0]}")
     else:
         us, gbs, how = res
         print(f"{args.op} {w.name}: {us:.1f} us per call, {gbs:.0f} GB/s ({how})")

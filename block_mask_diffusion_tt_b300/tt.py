@@ -64,6 +64,15 @@ BLOCK_LOGITS_FN = ctypes.CFUNCTYPE(ctypes.c_int, _p, _i32, _i32, _p, _p, _p, _p)
 BLOCK_KV_FN = ctypes.CFUNCTYPE(ctypes.c_int, _p, _i32, _p, _p, _p, _p, _p)
 
 
+STATE_MAX_LAYERS, STATE_MAX_PARTS = 64, 4
+_i64xP = ctypes.c_int64 * STATE_MAX_PARTS
+
+
+class StateDesc(ctypes.Structure):
+    _fields_ = [("B", _i32), ("n_layers", _i32), ("n_parts", _i32), ("bytes", _i64xP),
+                ("src_stride", _i64xP), ("dst_stride", _i64xP)]
+
+
 class GenerateParams(ctypes.Structure):
     _fields_ = [("max_new_tokens", _i32), ("eos_token_id", _i32), ("steps_per_block", _i32),
                 ("timeout_ms", _i32)]
@@ -101,6 +110,7 @@ def load(path: str = LIB_PATH):
                                            ctypes.c_float, ctypes.c_uint64, _p, _p]),
         "tt_synth_logits_producer": (ctypes.c_int, [_p, _i32, _p, _p, _p, _p]),
         "tt_kv_append": (ctypes.c_int, [ctypes.POINTER(KvDesc), _p, _p, _p, _p, _p, _p, _p, _p]),
+        "tt_mamba_state_seed": (ctypes.c_int, [ctypes.POINTER(StateDesc), _p, _p, _p, _p]),
         "tt_generate_blocks_workspace_size": (_sz, [ctypes.POINTER(UnmaskDesc)]),
         "tt_generate_blocks": (ctypes.c_int, [ctypes.POINTER(UnmaskDesc), ctypes.POINTER(KvDesc),
                                               ctypes.POINTER(GenerateParams), _p, _p, _p, _p,
@@ -403,6 +413,38 @@ def kv_append(k_ctx: list, v_ctx: list, ctx_lens, k_blk: list, v_blk: list, acti
                               ptrs[3], _ptr(active), _ptr(overflow), _stream(stream)))
 
 
+# ------------------------------------------------------------------ Mamba-2 state seeding
+def mamba_state_seed(src: list, dst: list, active=None, stream=None):
+    """Seeds the denoiser's Mamba-2 states from the context tower's (tt_mamba_state_seed).
+
+    src, dst: lists over layers of lists over parts (e.g. [conv, ssm]) of device
+    tensors [B, ...], each part with the same shape and strides in every layer;
+    active uint8[B] or None.
+    """
+    n_layers, n_parts = len(src), len(src[0])
+    if len(dst) != n_layers or any(len(x) != n_parts for x in src + dst):
+        raise ValueError("src and dst need the same layers and parts")
+    if not 1 <= n_layers <= STATE_MAX_LAYERS or not 1 <= n_parts <= STATE_MAX_PARTS:
+        raise ValueError("too many layers or parts")
+    B = src[0][0].shape[0]
+    desc = StateDesc(B=B, n_layers=n_layers, n_parts=n_parts)
+    for p in range(n_parts):
+        s0, d0 = src[0][p], dst[0][p]
+        for layer in range(n_layers):
+            for t, ref in ((src[layer][p], s0), (dst[layer][p], d0)):
+                if not t.is_cuda or t.shape != ref.shape or t.stride() != ref.stride() \
+                        or t.dtype != ref.dtype or not t[0].is_contiguous():
+                    raise ValueError("each part needs one shape, dtype and stride in every layer, "
+                                     "with each sequence's state contiguous")
+        desc.bytes[p] = s0[0].numel() * s0.element_size()
+        desc.src_stride[p] = s0.stride(0) * s0.element_size()
+        desc.dst_stride[p] = d0.stride(0) * d0.element_size()
+    arr = ctypes.c_void_p * (n_layers * n_parts)
+    sp = arr(*[src[l][p].data_ptr() for l in range(n_layers) for p in range(n_parts)])
+    dp = arr(*[dst[l][p].data_ptr() for l in range(n_layers) for p in range(n_parts)])
+    check(load().tt_mamba_state_seed(ctypes.byref(desc), sp, dp, _ptr(active), _stream(stream)))
+
+
 # ------------------------------------------------------------------ block-by-block generation
 def _kv_desc(k_ctx: list, k_blk: list) -> KvDesc:
     B, Hkv, Lmax, d = k_ctx[0].shape
@@ -490,4 +532,4 @@ def exported_symbols() -> list:
             "tt_confidence_unmask", "tt_confidence_unmask_error", "tt_block_init", "tt_denoise_block_loop_workspace_size",
             "tt_denoise_block_loop",
             "tt_synth_logits", "tt_synth_logits_producer", "tt_kv_append",
-            "tt_generate_blocks_workspace_size", "tt_generate_blocks"]
+            "tt_mamba_state_seed", "tt_generate_blocks_workspace_size", "tt_generate_blocks"]

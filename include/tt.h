@@ -382,6 +382,40 @@ tt_status tt_kv_append(const tt_kv_desc *desc, void *const *k_ctx, void *const *
                        int32_t *ctx_lens, const void *const *k_blk, const void *const *v_blk,
                        const uint8_t *active, int32_t *overflow, tt_stream_t stream);
 
+/* ---------------------------------------------------------- Mamba-2 state seeding
+ *
+ * The denoiser's Mamba-2 layers start from the context tower's states: each
+ * denoiser Mamba layer takes as its initial state the conv/SSM boundary state the
+ * corresponding context-tower layer ends on (dothoosh.com, "فرآیند انتشار در برابر
+ * رمزگشایی متوالی در مدل جدید انویدیا", architecture bullets; aitrends.kr,
+ * "Nemotron-Labs-TwoTower-30B-A3B-Base-BF16", section "technical features").  The
+ * pages give no recurrence; this is the seeding copy, for all layers in one launch.
+ */
+#define TT_STATE_MAX_LAYERS 64
+#define TT_STATE_MAX_PARTS 4
+
+typedef struct {
+    int32_t B;
+    int32_t n_layers;                       /* 1..TT_STATE_MAX_LAYERS */
+    int32_t n_parts;                        /* state tensors per layer (e.g. conv, SSM), 1..4 */
+    int64_t bytes[TT_STATE_MAX_PARTS];      /* bytes of one sequence's state of each part */
+    int64_t src_stride[TT_STATE_MAX_PARTS]; /* bytes between sequences in the source */
+    int64_t dst_stride[TT_STATE_MAX_PARTS]; /* bytes between sequences in the destination */
+} tt_state_desc;
+
+/*
+ * For every layer l, part p and sequence b taking part (active == NULL, or
+ * active[b] != 0): the bytes [0, bytes[p]) of src[l*n_parts + p] + b*src_stride[p]
+ * are copied to dst[l*n_parts + p] + b*dst_stride[p].  Sequences not taking part
+ * keep their destination state.
+ *   src, dst  host arrays of n_layers*n_parts device pointers (16-byte aligned);
+ *   bytes and strides positive multiples of 16, strides at least the size;
+ *   n_layers*n_parts*B at most 65535.  One launch; sources and destinations must
+ *   not overlap.
+ */
+tt_status tt_mamba_state_seed(const tt_state_desc *desc, const void *const *src,
+                              void *const *dst, const uint8_t *active, tt_stream_t stream);
+
 /* ------------------------------------------------------- block-by-block generation
  *
  * Blocks of S positions are generated one after another: each block is denoised by

@@ -186,3 +186,31 @@ def test_kv_append_rejects_bad_strides_and_pointers(lib):
     assert _kv_call(lib, _kv_desc()) == tt.TT_ERR_INVALID_ARG  # null pointers
     assert _kv_call(lib, _kv_desc(), ptr=0x100008) == tt.TT_ERR_INVALID_ARG  # not 16-byte aligned
     assert _kv_call(lib, _kv_desc(B=0)) == tt.TT_OK  # nothing to do: no launch
+
+
+def test_state_seed_rejects_bad_desc(lib):
+    desc = tt.StateDesc(B=2, n_layers=0, n_parts=1)
+    assert lib.tt_mamba_state_seed(ctypes.byref(desc), None, None, None, None) == tt.TT_ERR_INVALID_ARG
+    desc = tt.StateDesc(B=2, n_layers=1, n_parts=5)
+    assert lib.tt_mamba_state_seed(ctypes.byref(desc), None, None, None, None) == tt.TT_ERR_INVALID_ARG
+    desc = tt.StateDesc(B=2, n_layers=1, n_parts=1)
+    desc.bytes[0] = 24  # not a multiple of 16
+    desc.src_stride[0] = desc.dst_stride[0] = 32
+    arr = (ctypes.c_void_p * 1)(16)
+    assert lib.tt_mamba_state_seed(ctypes.byref(desc), arr, arr, None, None) == tt.TT_ERR_UNSUPPORTED
+    assert "multiple of 16" in tt.last_error()
+
+
+def test_generate_rejects_bad_params(lib):
+    desc = tt.unmask_desc(2, 16, 100, tt.TT_BF16, 0.1, 0.8, 3)
+    kv = tt.KvDesc(B=2, S=16, Hkv=2, d=64, Lmax=64, n_layers=1)
+    gp = tt.GenerateParams(max_new_tokens=0, eos_token_id=-1, steps_per_block=16, timeout_ms=0)
+    args = [None] * 17
+    st = lib.tt_generate_blocks(ctypes.byref(desc), ctypes.byref(kv), ctypes.byref(gp), *args[:15],
+                                None, 0, None, None)
+    assert st == tt.TT_ERR_INVALID_ARG
+    gp.max_new_tokens = 32
+    kv.S = 8  # block size differs from the unmask desc
+    st = lib.tt_generate_blocks(ctypes.byref(desc), ctypes.byref(kv), ctypes.byref(gp), *args[:15],
+                                None, 0, None, None)
+    assert st == tt.TT_ERR_INVALID_ARG and "B/S" in tt.last_error()
