@@ -399,11 +399,14 @@ __device__ void unmask_producer(const UnmaskArgs &p, const Ring &rg) {
                     mbar_expect_tx(full, bytes);
                     bulk_load(rg.stage(stage, unit_bytes),
                               x.rp + static_cast<size_t>(x.v0) * ESIZE, bytes, full, policy);
-                    issued |= 1u << stage;
-                    last_par = (last_par & ~(1u << stage)) | (phase << stage);
                 } else {
                     mbar_arrive(full);
                 }
+                // the phase posted last on each stage, with data or not: a later post
+                // without data moves the barrier on, so the drain below must wait for
+                // the last post's parity, not the last copy's
+                issued |= 1u << stage;
+                last_par = (last_par & ~(1u << stage)) | (phase << stage);
                 if (++stage == p.nst) {
                     stage = 0;
                     phase ^= 1;
@@ -412,10 +415,12 @@ __device__ void unmask_producer(const UnmaskArgs &p, const Ring &rg) {
         }
         ok = __shfl_sync(~0u, ok ? 1 : 0, 0) != 0;
     }
-    // no copy may still be landing when the CTA exits
+    // no copy may still be landing when the CTA exits: wait for the last phase posted
+    // on each stage (a phase posted without data is already complete)
     if (lane == 0)
         for (int st = 0; st < p.nst; ++st)
-            if (issued >> st & 1u) mbar_drain(rg.full(st), last_par >> st & 1u);
+            if ((issued >> st & 1u) && !mbar_drain(rg.full(st), last_par >> st & 1u))
+                atomicCAS(const_cast<int *>(rg.err), 0, kErrProducer);
 }
 
 // Consumer warp w takes eighth w of every unit of the CTA.  It waits for the unit's

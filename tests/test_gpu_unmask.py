@@ -144,3 +144,30 @@ def test_rows_with_negative_infinity():
     flat[1, 1::2] = -np.inf
     flat[2, :V - 1] = -np.inf   # one finite logit
     _gpu.check_unmask(logits, "f32", 0.1, 0.8)
+
+
+def test_rows_not_masked_cost_no_wait():
+    """A step where most rows are already committed: their units are posted without
+    data.  The call must finish promptly and leave the error word at 0 (every wait of
+    the kernel is bounded at 2 s and a wait that runs out sets the word)."""
+    import time
+    B, S, V = 16, 16, 131072
+    logits = synth.counter_logits(14, 0, B, S, V, 2.0, 0.6, "bf16")
+    rng = np.random.default_rng(14)
+    masked = (rng.random((B, S)) < 0.2).astype(np.uint8)
+    tokens = np.where(masked == 1, 3, 7).astype(np.int32)
+    desc = tt.unmask_desc(B, S, V, tt.TT_BF16, 0.1, 0.8, 3)
+    ws = tt.Workspace(tt.confidence_unmask_workspace_size(desc))
+    lg = _gpu.bf16_dev(logits)
+    for rep in range(3):
+        tok_d = torch.from_numpy(tokens.copy()).to(_gpu.DEV)
+        msk_d = torch.from_numpy(masked.copy()).to(_gpu.DEV)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        tt.confidence_unmask(lg, tok_d, msk_d, 0.1, 0.8, 3, workspace=ws)
+        torch.cuda.synchronize()
+        assert time.perf_counter() - t0 < 0.5
+    flag = ctypes.c_int32(-1)
+    tt.check(tt.load().tt_confidence_unmask_error(ws.ptr, ctypes.byref(flag), None))
+    assert flag.value == 0
+    _gpu.check_unmask(logits, "bf16", 0.1, 0.8, tokens=tokens, masked=masked)
