@@ -66,8 +66,10 @@ constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kRescaleLog2 = 8.f;  // lazy rescale: O is rescaled when the max grows by > 2^8
 constexpr int kTmemCols = 512;
 // Bits of the workspace error word: a role that gave up on a wait (bit role-1:
-// 1 TMA producer, 2 MMA issuer, 4 softmax warps) and a context length outside [0, Lmax].
+// 1 TMA producer, 2 MMA issuer, 4 softmax warps), a context length outside [0, Lmax],
+// and a page of a paged cache outside the pool.
 constexpr int kErrCtxLen = 8;
+constexpr int kErrPage = 16;
 
 template <int D>
 struct Cfg {
@@ -109,6 +111,12 @@ struct AttnArgs {
     float2 *part_ml;  // [slots][256]
     int2 *pair_split;  // [npairs]: first and last CTA of each pair's tile range
     int *err_word;
+    int keys;                  // TT_KEYS_ALL / _PREFIX / _BLOCK
+    const int32_t *page_of;    // paged cache: [B, max_pages] page of each 64-key tile, or null
+    int max_pages, n_pages;
+    const float *q_scale;      // modulation: q' = q (1 + scale) + shift, [B, Hq, D] fp32, or null
+    const float *q_shift;
+    const float *o_gate;       // out = gate * attention, [B, Hq, D] fp32, or null
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -285,8 +293,10 @@ struct Sched {
             const int bg = p / a.NRG;
             s.g = bg % a.Hkv;
             s.b = bg / a.Hkv;
-            // the context length comes from shared memory (no global read here)
-            s.nctx = static_cast<int>(pe - rs) - 1;
+            // the context length comes from shared memory (no global read here); a pair
+            // attending to the prefix only has no block tile (and one empty tile when
+            // its prefix is empty)
+            s.nctx = static_cast<int>(pe - rs) - (a.keys == TT_KEYS_PREFIX ? 0 : 1);
             s.L = s.nctx == 0 ? 0 : (s.nctx - 1) * kTN + tail[p];
             s.rows = min(kRows, a.R - s.rg * kRows);
             s.nh = s.rows > 128 ? 2 : 1;
@@ -299,6 +309,23 @@ struct Sched {
         return false;
     }
 };
+
+// Prefix length of pair p's sequence, clamped into [0, Lmax] (a value outside is
+// recorded in the error word when `flag`), and 0 when only the block's keys count.
+__device__ __forceinline__ int pair_len(const AttnArgs &a, int p, bool flag) {
+    int L = a.lens[p / (a.Hkv * a.NRG)];
+    if (L < 0 || L > a.Lmax) {
+        if (flag) atomicOr(a.err_word, kErrCtxLen);
+        L = L < 0 ? 0 : a.Lmax;
+    }
+    return a.keys == TT_KEYS_BLOCK ? 0 : L;
+}
+// 64-key tiles of a pair: the prefix tiles, plus the block tile unless only the prefix
+// counts (then at least one tile, empty when the prefix is).
+__device__ __forceinline__ int pair_tiles(const AttnArgs &a, int L) {
+    const int nctx = (L + kTN - 1) / kTN;
+    return a.keys == TT_KEYS_PREFIX ? (nctx > 0 ? nctx : 1) : nctx + 1;
+}
 
 __device__ __forceinline__ int tile_valid(const AttnArgs &a, const Seg &s, int tile) {
     return tile == s.nctx ? a.S : min(kTN, s.L - tile * kTN);
@@ -324,6 +351,20 @@ struct Smem {
     __device__ uint32_t q_tile(int h) const { return qbuf + h * Cfg<D>::kQHalfBytes; }
 };
 
+// Page of context tile `tile` of sequence b in a paged cache.  Tiles holding no key
+// of the prefix (an empty prefix's one tile) need no page; a page id outside the
+// pool is recorded in the error word and replaced by n_pages, past the map's end, so
+// the TMA load reads the fill value instead of another sequence's keys.
+__device__ __forceinline__ int page_at(const AttnArgs &a, int b, int tile, int L) {
+    if (tile * kTN >= L) return a.n_pages;
+    const int pg = __ldg(a.page_of + static_cast<int64_t>(b) * a.max_pages + tile);
+    if (pg < 0 || pg >= a.n_pages) {
+        atomicOr(a.err_word, kErrPage);
+        return a.n_pages;
+    }
+    return pg;
+}
+
 template <int D>
 __device__ void role_producer(const AttnArgs &a, Sched sch, const Smem<D> &sm,
                               const CUtensorMap *tkc, const CUtensorMap *tvc,
@@ -336,22 +377,34 @@ __device__ void role_producer(const AttnArgs &a, Sched sch, const Smem<D> &sm,
     const uint64_t policy = l2_evict_first();
     Seg s;
     bool ok = true;
+    int next_page = 0;  // paged cache: page of the next context tile, read one tile ahead
     while (ok && sch.next(a, s)) {
+        if (a.page_of && s.tile0 < s.nctx) next_page = page_at(a, s.b, s.tile0, s.L);
         for (int it = 0; it < s.ntiles; ++it) {
             if (!mbar_wait(sm.empty(stage), phase ^ 1, sm.err, 1)) { ok = false; break; }
             const uint32_t full = sm.full(stage);
             mbar_expect_tx(full, C::kStageBytes);
             const int tile = s.tile0 + it;
             const bool blk = tile == s.nctx;
-            // ctx maps: (d, Lmax, Hkv, B); block maps: (d, Hkv, S, B)
+            // ctx maps: (d, Lmax, Hkv, B), or for a paged cache (d, 64, Hkv, n_pages);
+            // block maps: (d, Hkv, S, B)
             const CUtensorMap *mk = blk ? tkb : tkc;
             const CUtensorMap *mv = blk ? tvb : tvc;
-            const int c1 = blk ? s.g : tile * kTN, c2 = blk ? 0 : s.g;
+            int c1 = blk ? s.g : tile * kTN, c3 = s.b;
+            if (!blk && a.page_of) {
+                // the tile's page (a page outside the pool is flagged and read as the
+                // fill value: the coordinate n_pages lies past the map)
+                c1 = 0;
+                c3 = next_page;
+                if (it + 1 < s.ntiles && tile + 1 < s.nctx)
+                    next_page = page_at(a, s.b, tile + 1, s.L);
+            }
+            const int c2 = blk ? 0 : s.g;
             const uint32_t sb = sm.stages + stage * C::kStageBytes;
 #pragma unroll
             for (int c = 0; c < C::kChunks; ++c) {
-                tma_load_4d(sb + c * C::kRegionBytes, mk, c * 64, c1, c2, s.b, full, policy);
-                tma_load_4d(sb + (C::kChunks + c) * C::kRegionBytes, mv, c * 64, c1, c2, s.b, full,
+                tma_load_4d(sb + c * C::kRegionBytes, mk, c * 64, c1, c2, c3, full, policy);
+                tma_load_4d(sb + (C::kChunks + c) * C::kRegionBytes, mv, c * 64, c1, c2, c3, full,
                             policy);
             }
             issued |= 1u << stage;
@@ -463,11 +516,23 @@ __device__ void role_mma(const AttnArgs &a, Sched sch, const Smem<D> &sm, uint32
 }
 
 template <int D>
-__device__ __forceinline__ void store_row(const AttnArgs &a, const Seg &s, int rl,
-                                          const float *o, int col0) {
+__device__ __forceinline__ void store_row(const AttnArgs &a, const Seg &s, int rl, float *o,
+                                          int col0) {
     const int rr = s.rg * kRows + rl;
     const int sq = rr / a.G, head = s.g * a.G + rr % a.G;
     uint16_t *dst = a.out + s.b * a.os[0] + sq * a.os[1] + head * a.os[2] + col0;
+    if (a.o_gate) {  // adaLN-single gate of the attention output, [B, Hq, D]
+        const float4 *gp = reinterpret_cast<const float4 *>(
+            a.o_gate + (static_cast<int64_t>(s.b) * a.Hq + head) * D + col0);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float4 gv = __ldg(gp + j);
+            o[4 * j] *= gv.x;
+            o[4 * j + 1] *= gv.y;
+            o[4 * j + 2] *= gv.z;
+            o[4 * j + 3] *= gv.w;
+        }
+    }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         uint4 v;
@@ -484,7 +549,8 @@ __device__ __forceinline__ void store_lse(const AttnArgs &a, const Seg &s, int r
     if (!a.lse) return;
     const int rr = s.rg * kRows + rl;
     const int sq = rr / a.G, head = s.g * a.G + rr % a.G;
-    a.lse[(static_cast<int64_t>(s.b) * a.Hq + head) * a.S + sq] = (m_log2 + __log2f(l)) * kLn2;
+    a.lse[(static_cast<int64_t>(s.b) * a.Hq + head) * a.S + sq] =
+        l > 0.f ? (m_log2 + __log2f(l)) * kLn2 : -INFINITY;  // no key: empty sum
 }
 
 template <int D>
@@ -517,6 +583,24 @@ __device__ void role_softmax(const AttnArgs &a, Sched sch, const Smem<D> &sm, ui
                                                                sq * a.qs[1] + head * a.qs[2]);
 #pragma unroll
             for (int j = 0; j < D / 8; ++j) qv[j] = __ldg(src + j);
+            if (a.q_scale) {  // adaLN-single: q' = q (1 + scale) + shift, rounded to bf16
+                const int64_t mo = (static_cast<int64_t>(q_seg.b) * a.Hq + head) * D;
+                const float4 *sc = reinterpret_cast<const float4 *>(a.q_scale + mo);
+                const float4 *sh = reinterpret_cast<const float4 *>(a.q_shift + mo);
+#pragma unroll
+                for (int j = 0; j < D / 8; ++j) {
+                    const float4 s0 = __ldg(sc + 2 * j), s1 = __ldg(sc + 2 * j + 1);
+                    const float4 h0 = __ldg(sh + 2 * j), h1 = __ldg(sh + 2 * j + 1);
+                    qv[j].x = pack_bf16x2(fmaf(bf16_lo(qv[j].x), 1.f + s0.x, h0.x),
+                                          fmaf(bf16_hi(qv[j].x), 1.f + s0.y, h0.y));
+                    qv[j].y = pack_bf16x2(fmaf(bf16_lo(qv[j].y), 1.f + s0.z, h0.z),
+                                          fmaf(bf16_hi(qv[j].y), 1.f + s0.w, h0.w));
+                    qv[j].z = pack_bf16x2(fmaf(bf16_lo(qv[j].z), 1.f + s1.x, h1.x),
+                                          fmaf(bf16_hi(qv[j].z), 1.f + s1.y, h1.y));
+                    qv[j].w = pack_bf16x2(fmaf(bf16_lo(qv[j].w), 1.f + s1.z, h1.z),
+                                          fmaf(bf16_hi(qv[j].w), 1.f + s1.w, h1.w));
+                }
+            }
         } else {
 #pragma unroll
             for (int j = 0; j < D / 8; ++j) qv[j] = make_uint4(0u, 0u, 0u, 0u);
@@ -569,7 +653,9 @@ __device__ void role_softmax(const AttnArgs &a, Sched sch, const Smem<D> &sm, ui
             const float mx = tile_max(v);
             if (it == 0) m_run = mx * c;
             uint32_t pk[kTN / 2];
-            float lsum = exp_tile(v, c, m_run, pk);
+            // a tile without a key (an empty prefix attended alone) has max -inf: its
+            // P is 0 whatever the reference, and 0 keeps the arithmetic finite
+            float lsum = exp_tile(v, c, m_run == -INFINITY ? 0.f : m_run, pk);
             if (s.nh == 2) mbar_arrive_after(sm.turn(h ^ 1), lsum);
             if (it > 0) {
                 const float m_tile = mx * c;
@@ -611,7 +697,7 @@ __device__ void role_softmax(const AttnArgs &a, Sched sch, const Smem<D> &sm, ui
         if (!wait_pv(cnt - 1)) { ok = false; break; }
         tc_fence_after();
         if (s.c_first == s.c_last) {
-            const float inv = 1.f / l_run;
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;  // no key at all: output 0
 #pragma unroll 1
             for (int j = 0; j < D / 32; ++j) {
                 uint32_t o[32];
@@ -629,7 +715,7 @@ __device__ void role_softmax(const AttnArgs &a, Sched sch, const Smem<D> &sm, ui
             // ---- split pair: write this CTA's partial (O / l, m, l); block_attn_merge_kernel
             // combines the partials once the whole grid has finished
             const size_t slot = static_cast<size_t>(blockIdx.x + s.p);
-            const float inv = 1.f / l_run;
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll 1
             for (int j = 0; j < D / 32; ++j) {
                 uint32_t o[32];
@@ -673,14 +759,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int p0 = min(a.npairs, t * per), p1 = min(a.npairs, p0 + per);
         int local = 0;
         for (int p = p0; p < p1; ++p) {
-            int L = a.lens[p / (a.Hkv * a.NRG)];
-            // a length outside [0, Lmax] is recorded in the error word and clamped, so
-            // no read leaves the cache
-            if (L < 0 || L > a.Lmax) {
-                if (blockIdx.x == 0) atomicOr(a.err_word, kErrCtxLen);
-                L = L < 0 ? 0 : a.Lmax;
-            }
-            local += (L + kTN - 1) / kTN + 1 + kSegCost;
+            const int L = pair_len(a, p, blockIdx.x == 0);
+            local += pair_tiles(a, L) + kSegCost;
         }
         int incl = local;
 #pragma unroll
@@ -703,11 +783,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         int run = incl - local + (warp > 0 ? warp_sums[warp - 1] : 0);
         for (int p = p0; p < p1; ++p) {
             prefix[p] = run;
-            int L = a.lens[p / (a.Hkv * a.NRG)];
-            L = L < 0 ? 0 : (L > a.Lmax ? a.Lmax : L);
+            const int L = pair_len(a, p, false);
             const int nctx = (L + kTN - 1) / kTN;
             tail[p] = static_cast<uint8_t>(nctx == 0 ? 0 : L - (nctx - 1) * kTN);
-            run += nctx + 1 + kSegCost;
+            run += pair_tiles(a, L) + kSegCost;
         }
         if (t == kThreads - 1) prefix[a.npairs] = run;
         __syncthreads();
@@ -839,7 +918,7 @@ __global__ void __launch_bounds__(kMergeThreads, 4) block_attn_merge_kernel(cons
         }
 #pragma unroll
         for (int i = 0; i < kMergeBatch; ++i) {
-            if (c0 + i <= cs.y) {
+            if (c0 + i <= cs.y && ml[i].x != -INFINITY) {  // a partial without keys adds nothing
                 const float Mn = fmaxf(M, ml[i].x);
                 const float so = ex2_approx(M - Mn), w = ex2_approx(ml[i].x - Mn) * ml[i].y;
                 M = Mn;
@@ -849,11 +928,18 @@ __global__ void __launch_bounds__(kMergeThreads, 4) block_attn_merge_kernel(cons
             }
         }
     }
-    const float inv = 1.f / den;
+    const float inv = den > 0.f ? 1.f / den : 0.f;
     const int rr = rg * kRows + rl;
     const int bg = p / a.NRG, g = bg % a.Hkv, b = bg / a.Hkv;
     const int sq = rr / a.G, head = g * a.G + rr % a.G;
     uint16_t *dst = a.out + b * a.os[0] + sq * a.os[1] + head * a.os[2] + col0;
+    if (a.o_gate) {  // adaLN-single gate of the attention output, [B, Hq, D]
+        const float4 *gp = reinterpret_cast<const float4 *>(
+            a.o_gate + (static_cast<int64_t>(b) * a.Hq + head) * D + col0);
+        const float4 g0 = __ldg(gp), g1 = __ldg(gp + 1);
+        acc[0] *= g0.x; acc[1] *= g0.y; acc[2] *= g0.z; acc[3] *= g0.w;
+        acc[4] *= g1.x; acc[5] *= g1.y; acc[6] *= g1.z; acc[7] *= g1.w;
+    }
     uint4 o;
     o.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
     o.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
@@ -861,7 +947,8 @@ __global__ void __launch_bounds__(kMergeThreads, 4) block_attn_merge_kernel(cons
     o.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
     *reinterpret_cast<uint4 *>(dst) = o;
     if (col0 == 0 && a.lse)
-        a.lse[(static_cast<int64_t>(b) * a.Hq + head) * a.S + sq] = (M + __log2f(den)) * kLn2;
+        a.lse[(static_cast<int64_t>(b) * a.Hq + head) * a.S + sq] =
+            den > 0.f ? (M + __log2f(den)) * kLn2 : -INFINITY;
 }
 
 // ---------------------------------------------------------------- host
@@ -968,7 +1055,7 @@ tt_status make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, u
 // (a decode loop calls every layer with the same caches step after step).
 struct MapKey {
     const void *k_ctx, *v_ctx, *k_blk, *v_blk;
-    int32_t B, S, Hkv, Lmax, d;
+    int32_t B, S, Hkv, Lmax, d, n_pages;  // n_pages > 0: paged context pools
     int64_t kc[4], vc[4], kb[4], vb[4];
     bool operator==(const MapKey &o) const { return memcmp(this, &o, sizeof(MapKey)) == 0; }
 };
@@ -981,21 +1068,25 @@ constexpr int kMapCache = 16;
 
 template <int D>
 tt_status encode_maps(const tt_attn_desc *d, const void *k_ctx, const void *v_ctx, const void *k_blk,
-                      const void *v_blk, MapEntry *e, const char *fn) {
+                      const void *v_blk, int n_pages, MapEntry *e, const char *fn) {
     tt_status st;
-    const uint64_t B = d->B, S = d->S, Hkv = d->Hkv, Lmax = d->Lmax;
+    const uint64_t B = d->B, S = d->S, Hkv = d->Hkv;
+    // a paged cache is a pool [n_pages, Hkv, 64, d]: the map's rows are a page's 64 keys
+    // and its outer dimension the page; otherwise [B, Hkv, Lmax, d]
+    const uint64_t Lmax = n_pages > 0 ? kTN : d->Lmax;
+    const uint64_t outer = n_pages > 0 ? static_cast<uint64_t>(n_pages) : B;
     if ((st = make_map(&e->kb, k_blk, D, Hkv, S, B, d->kblk_strides[2], d->kblk_strides[1],
                        d->kblk_strides[0], 1, 64, fn, "k_blk")) != TT_OK)
         return st;
     if ((st = make_map(&e->vb, v_blk, D, Hkv, S, B, d->vblk_strides[2], d->vblk_strides[1],
                        d->vblk_strides[0], 1, 64, fn, "v_blk")) != TT_OK)
         return st;
-    if (Lmax > 0) {
-        if ((st = make_map(&e->kc, k_ctx, D, Lmax, Hkv, B, d->kctx_strides[2], d->kctx_strides[1],
-                           d->kctx_strides[0], 64, 1, fn, "k_ctx")) != TT_OK)
+    if (d->Lmax > 0) {
+        if ((st = make_map(&e->kc, k_ctx, D, Lmax, Hkv, outer, d->kctx_strides[2],
+                           d->kctx_strides[1], d->kctx_strides[0], 64, 1, fn, "k_ctx")) != TT_OK)
             return st;
-        if ((st = make_map(&e->vc, v_ctx, D, Lmax, Hkv, B, d->vctx_strides[2], d->vctx_strides[1],
-                           d->vctx_strides[0], 64, 1, fn, "v_ctx")) != TT_OK)
+        if ((st = make_map(&e->vc, v_ctx, D, Lmax, Hkv, outer, d->vctx_strides[2],
+                           d->vctx_strides[1], d->vctx_strides[0], 64, 1, fn, "v_ctx")) != TT_OK)
             return st;
     } else {  // no context rows: the context maps are never used
         e->kc = e->kb;
@@ -1008,12 +1099,14 @@ tt_status encode_maps(const tt_attn_desc *d, const void *k_ctx, const void *v_ct
 template <int D>
 tt_status launch(const tt_attn_desc *d, const AttnArgs &a, const void *k_ctx, const void *v_ctx,
                  const void *k_blk, const void *v_blk, cudaStream_t stream, const char *fn) {
+    const int n_pages = a.page_of ? a.n_pages : 0;
     thread_local MapEntry cache[kMapCache] = {};
     thread_local int next_slot = 0;
     MapKey key;
     memset(&key, 0, sizeof key);
     key.k_ctx = k_ctx; key.v_ctx = v_ctx; key.k_blk = k_blk; key.v_blk = v_blk;
     key.B = d->B; key.S = d->S; key.Hkv = d->Hkv; key.Lmax = d->Lmax; key.d = d->d;
+    key.n_pages = n_pages;
     memcpy(key.kc, d->kctx_strides, sizeof key.kc);
     memcpy(key.vc, d->vctx_strides, sizeof key.vc);
     memcpy(key.kb, d->kblk_strides, sizeof key.kb);
@@ -1022,7 +1115,8 @@ tt_status launch(const tt_attn_desc *d, const AttnArgs &a, const void *k_ctx, co
     for (int i = 0; i < kMapCache && !hit; ++i)
         if (cache[i].used && cache[i].key == key) hit = &cache[i];
     if (!hit) {
-        tt_status st = encode_maps<D>(d, k_ctx, v_ctx, k_blk, v_blk, &cache[next_slot], fn);
+        tt_status st =
+            encode_maps<D>(d, k_ctx, v_ctx, k_blk, v_blk, n_pages, &cache[next_slot], fn);
         if (st != TT_OK) return st;
         cache[next_slot].key = key;
         cache[next_slot].used = true;
@@ -1076,10 +1170,39 @@ tt_status check_ptrs(const tt_attn_desc *d, const void *q, const void *k_ctx, co
     return TT_OK;
 }
 
-tt_status run(const tt_attn_desc *d, const Geometry &g, const AttnWs &w, const void *q,
-              const void *k_ctx, const void *v_ctx, const int32_t *ctx_lens, const void *k_blk,
-              const void *v_blk, void *out, float *lse, cudaStream_t stream, const char *fn) {
+tt_status check_opts(const tt_attn_desc *d, const tt_attn_opts *o, const char *fn) {
+    if (!o) return TT_OK;
+    if (o->keys != TT_KEYS_ALL && o->keys != TT_KEYS_PREFIX && o->keys != TT_KEYS_BLOCK)
+        return fail(TT_ERR_INVALID_ARG, "%s: unknown key set %d", fn, o->keys);
+    if (o->block_table) {
+        if (o->max_pages < 1 || o->n_pages < 1)
+            return fail(TT_ERR_INVALID_ARG, "%s: paged cache needs max_pages and n_pages >= 1", fn);
+        if (static_cast<int64_t>(o->max_pages) * kTN != d->Lmax)
+            return fail(TT_ERR_INVALID_ARG, "%s: paged cache needs Lmax = max_pages * 64", fn);
+        if (reinterpret_cast<uintptr_t>(o->block_table) % 4)
+            return fail(TT_ERR_INVALID_ARG, "%s: block table not 4-byte aligned", fn);
+    }
+    if ((o->q_scale == nullptr) != (o->q_shift == nullptr))
+        return fail(TT_ERR_INVALID_ARG, "%s: q_scale and q_shift go together", fn);
+    const void *m[3] = {o->q_scale, o->q_shift, o->o_gate};
+    for (int i = 0; i < 3; ++i)
+        if (m[i] && reinterpret_cast<uintptr_t>(m[i]) % 16)
+            return fail(TT_ERR_INVALID_ARG, "%s: modulation vectors not 16-byte aligned", fn);
+    return TT_OK;
+}
+
+tt_status run(const tt_attn_desc *d, const tt_attn_opts *o, const Geometry &g, const AttnWs &w,
+              const void *q, const void *k_ctx, const void *v_ctx, const int32_t *ctx_lens,
+              const void *k_blk, const void *v_blk, void *out, float *lse, cudaStream_t stream,
+              const char *fn) {
     AttnArgs a;
+    a.keys = o ? o->keys : TT_KEYS_ALL;
+    a.page_of = o ? o->block_table : nullptr;
+    a.max_pages = o ? o->max_pages : 0;
+    a.n_pages = o ? o->n_pages : 0;
+    a.q_scale = o ? o->q_scale : nullptr;
+    a.q_shift = o ? o->q_shift : nullptr;
+    a.o_gate = o ? o->o_gate : nullptr;
     a.q = static_cast<const uint16_t *>(q);
     a.out = static_cast<uint16_t *>(out);
     a.lse = lse;
@@ -1137,7 +1260,30 @@ tt_status tt_block_attn(const tt_attn_desc *d, const void *q, const void *k_ctx,
                     w.bytes);
     if (reinterpret_cast<uintptr_t>(workspace) % 256)
         return fail(TT_ERR_WORKSPACE, "%s: workspace not 256-byte aligned", fn);
-    return run(d, g, w, q, k_ctx, v_ctx, ctx_lens, k_blk, v_blk, out, lse, (cudaStream_t)stream, fn);
+    return run(d, nullptr, g, w, q, k_ctx, v_ctx, ctx_lens, k_blk, v_blk, out, lse,
+               (cudaStream_t)stream, fn);
+}
+
+tt_status tt_block_attn_ex(const tt_attn_desc *d, const tt_attn_opts *opts, const void *q,
+                           const void *k_ctx, const void *v_ctx, const int32_t *ctx_lens,
+                           const void *k_blk, const void *v_blk, void *out, float *lse,
+                           void *workspace, size_t workspace_bytes, tt_stream_t stream) {
+    const char *fn = "tt_block_attn_ex";
+    Geometry g;
+    tt_status st = validate(d, &g, fn);
+    if (st != TT_OK) return st;
+    if ((st = check_opts(d, opts, fn)) != TT_OK) return st;
+    if (d->B == 0) return TT_OK;
+    if ((st = check_ptrs(d, q, k_ctx, v_ctx, ctx_lens, k_blk, v_blk, out, lse, fn)) != TT_OK)
+        return st;
+    AttnWs w = carve(workspace, g.npairs, static_cast<size_t>(g.P) + g.npairs, d->d);
+    if (!workspace || workspace_bytes < w.bytes)
+        return fail(TT_ERR_WORKSPACE, "%s: workspace of %zu bytes, %zu needed", fn, workspace_bytes,
+                    w.bytes);
+    if (reinterpret_cast<uintptr_t>(workspace) % 256)
+        return fail(TT_ERR_WORKSPACE, "%s: workspace not 256-byte aligned", fn);
+    return run(d, opts, g, w, q, k_ctx, v_ctx, ctx_lens, k_blk, v_blk, out, lse,
+               (cudaStream_t)stream, fn);
 }
 
 tt_status tt_block_attn_error(const void *workspace, int32_t *flag_out, tt_stream_t stream) {
@@ -1214,5 +1360,6 @@ extern "C" tt_status tt_block_attn_noalloc(const tt_attn_desc *d, const void *q,
     const size_t head = reinterpret_cast<char *>(w.part_ml) - reinterpret_cast<char *>(base);
     st = cuda_status(cudaMemsetAsync(base, 0, head, (cudaStream_t)stream), fn);
     if (st != TT_OK) return st;
-    return run(d, g, w, q, k_ctx, v_ctx, ctx_lens, k_blk, v_blk, out, lse, (cudaStream_t)stream, fn);
+    return run(d, nullptr, g, w, q, k_ctx, v_ctx, ctx_lens, k_blk, v_blk, out, lse,
+               (cudaStream_t)stream, fn);
 }

@@ -42,6 +42,14 @@ class AttnDesc(ctypes.Structure):
                 ("vblk_strides", _i64x4), ("o_strides", _i64x4)]
 
 
+TT_KEYS_ALL, TT_KEYS_PREFIX, TT_KEYS_BLOCK = 0, 1, 2
+
+
+class AttnOpts(ctypes.Structure):
+    _fields_ = [("keys", _i32), ("block_table", _p), ("max_pages", _i32), ("n_pages", _i32),
+                ("q_scale", _p), ("q_shift", _p), ("o_gate", _p)]
+
+
 class UnmaskDesc(ctypes.Structure):
     _fields_ = [("B", _i32), ("S", _i32), ("V", _i32), ("logits_dtype", ctypes.c_int),
                 ("logits_row_stride", ctypes.c_int64), ("temperature", ctypes.c_float),
@@ -97,6 +105,10 @@ def load(path: str = LIB_PATH):
         "tt_block_attn": (ctypes.c_int, [ctypes.POINTER(AttnDesc), _p, _p, _p, _p, _p, _p, _p, _p,
                                          _p, _sz, _p]),
         "tt_block_attn_error": (ctypes.c_int, [_p, ctypes.POINTER(_i32), _p]),
+        "tt_block_attn_ex": (ctypes.c_int, [ctypes.POINTER(AttnDesc), ctypes.POINTER(AttnOpts), _p,
+                                            _p, _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
+        "tt_attn_lse_combine": (ctypes.c_int, [_i32, _i32, _i32, _i32, _p, _p, _p, _p, _p, _p,
+                                               _p]),
         "tt_confidence_unmask_workspace_size": (_sz, [ctypes.POINTER(UnmaskDesc)]),
         "tt_confidence_unmask": (ctypes.c_int, [ctypes.POINTER(UnmaskDesc), _p, _p, _p, _p, _p, _p,
                                                 _i32, _p, _sz, _p]),
@@ -215,6 +227,61 @@ def block_attn(q, k_ctx, v_ctx, ctx_lens, k_blk, v_blk, out=None, lse=None, scal
     check(load().tt_block_attn(ctypes.byref(desc), _ptr(q), _ptr(k_ctx), _ptr(v_ctx),
                                _ptr(ctx_lens), _ptr(k_blk), _ptr(v_blk), _ptr(out), _ptr(lse),
                                workspace.ptr, workspace.nbytes, _stream(stream)))
+    return out
+
+
+def block_attn_ex(q, k_ctx, v_ctx, ctx_lens, k_blk, v_blk, keys: int = TT_KEYS_ALL,
+                  block_table=None, n_pages: int = 0, q_scale=None, q_shift=None, o_gate=None,
+                  out=None, lse=None, scale: float = 0.0, workspace: Optional[Workspace] = None,
+                  stream=None):
+    """Block-query attention with options (tt_block_attn_ex).
+
+    keys: TT_KEYS_ALL / TT_KEYS_PREFIX / TT_KEYS_BLOCK.  block_table int32 [B, max_pages]
+    selects the paged cache: k_ctx / v_ctx are then pools [n_pages, Hkv, 64, d].
+    q_scale, q_shift, o_gate: fp32 [B, Hq, d] adaLN-single modulation.
+    """
+    for t, n, nd in ((q, "q", 4), (k_ctx, "k_ctx", 4), (v_ctx, "v_ctx", 4), (k_blk, "k_blk", 4),
+                     (v_blk, "v_blk", 4)):
+        _need(t, n, torch.bfloat16, nd)
+    _need(ctx_lens, "ctx_lens", torch.int32, 1)
+    for t, n in ((q_scale, "q_scale"), (q_shift, "q_shift"), (o_gate, "o_gate")):
+        if t is not None:
+            _need(t, n, torch.float32, 3)
+            if not t.is_contiguous():
+                raise ValueError(f"{n} must be contiguous [B, Hq, d]")
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    desc = attn_desc(q, k_ctx, v_ctx, k_blk, v_blk, out, scale)
+    opts = AttnOpts(keys=int(keys))
+    if block_table is not None:
+        _need(block_table, "block_table", torch.int32, 2)
+        opts.block_table = block_table.data_ptr()
+        opts.max_pages = block_table.shape[1]
+        opts.n_pages = int(n_pages) if n_pages else k_ctx.shape[0]
+        desc.Lmax = opts.max_pages * 64
+        desc.Hkv = k_ctx.shape[1]
+    for name, t in (("q_scale", q_scale), ("q_shift", q_shift), ("o_gate", o_gate)):
+        if t is not None:
+            setattr(opts, name, t.data_ptr())
+    if workspace is None:
+        workspace = Workspace(block_attn_workspace_size(desc), q.device)
+    check(load().tt_block_attn_ex(ctypes.byref(desc), ctypes.byref(opts), _ptr(q), _ptr(k_ctx),
+                                  _ptr(v_ctx), _ptr(ctx_lens), _ptr(k_blk), _ptr(v_blk), _ptr(out),
+                                  _ptr(lse), workspace.ptr, workspace.nbytes, _stream(stream)))
+    return out
+
+
+def attn_lse_combine(o1, lse1, o2, lse2, out=None, lse_out=None, stream=None):
+    """Joins two attention results over disjoint key sets (tt_attn_lse_combine)."""
+    B, S, Hq, d = o1.shape
+    for t in (o1, o2):
+        _need(t, "o", torch.bfloat16, 4)
+        if not t.is_contiguous():
+            raise ValueError("o1 and o2 must be contiguous")
+    if out is None:
+        out = torch.empty_like(o1)
+    check(load().tt_attn_lse_combine(B, S, Hq, d, _ptr(o1), _ptr(lse1), _ptr(o2), _ptr(lse2),
+                                     _ptr(out), _ptr(lse_out), _stream(stream)))
     return out
 
 
@@ -532,4 +599,5 @@ def exported_symbols() -> list:
             "tt_confidence_unmask", "tt_confidence_unmask_error", "tt_block_init", "tt_denoise_block_loop_workspace_size",
             "tt_denoise_block_loop",
             "tt_synth_logits", "tt_synth_logits_producer", "tt_kv_append",
-            "tt_mamba_state_seed", "tt_generate_blocks_workspace_size", "tt_generate_blocks"]
+            "tt_mamba_state_seed", "tt_generate_blocks_workspace_size", "tt_generate_blocks",
+            "tt_block_attn_ex", "tt_attn_lse_combine"]

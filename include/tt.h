@@ -155,12 +155,73 @@ tt_status tt_block_attn(const tt_attn_desc *desc, const void *q, const void *k_c
                         size_t workspace_bytes, tt_stream_t stream);
 
 /*
+ * Options of tt_block_attn_ex (a NULL options pointer, or all fields 0, is
+ * tt_block_attn):
+ *   keys      which keys every block query attends to, through one softmax:
+ *             TT_KEYS_ALL the prefix and the block (tt_block_attn); TT_KEYS_PREFIX
+ *             the context prefix only; TT_KEYS_BLOCK the block's own keys only.  The
+ *             aitrends.kr page ("Nemotron-Labs-TwoTower-30B-A3B-Base-BF16", section
+ *             "technical features") names in-block self-attention and layer-aligned
+ *             attention to the context separately: the two key sets attended apart,
+ *             each with its log-sum-exp, combine into the one softmax over both
+ *             (tt_attn_lse_combine).  A row with no key (TT_KEYS_PREFIX and L_b = 0)
+ *             gets out = 0 and lse = -inf.
+ *   block_table, max_pages, n_pages
+ *             a paged context cache: k_ctx and v_ctx are pools of n_pages pages of 64
+ *             keys, [n_pages, Hkv, 64, d] with kctx_strides/vctx_strides giving (page,
+ *             head, row, 1); block_table is device int32 [B, max_pages], entry j the
+ *             page that holds keys 64j .. 64j+63 of sequence b; desc->Lmax must be
+ *             max_pages * 64.  Entries past a sequence's length are not read.  A page
+ *             id outside [0, n_pages) is recorded (flag 16 of the error word) and read
+ *             as zeros.  NULL: the contiguous [B, Hkv, Lmax, d] cache.
+ *   q_scale, q_shift, o_gate
+ *             adaLN-single modulation (aitrends.kr page, technical features: scale,
+ *             shift and gate injected per timestep into each denoiser layer; dothoosh.com
+ *             page, architecture bullets), device fp32 [B, Hq, d] each: queries become
+ *             q * (1 + q_scale) + q_shift (rounded to bf16) before the scores, and the
+ *             output is multiplied by o_gate.  q_scale and q_shift go together; NULL
+ *             for none.  16-byte aligned.
+ */
+typedef enum { TT_KEYS_ALL = 0, TT_KEYS_PREFIX = 1, TT_KEYS_BLOCK = 2 } tt_attn_keys;
+
+typedef struct {
+    int32_t keys;
+    const int32_t *block_table;
+    int32_t max_pages;
+    int32_t n_pages;
+    const float *q_scale;
+    const float *q_shift;
+    const float *o_gate;
+} tt_attn_opts;
+
+/* tt_block_attn with options (see tt_attn_opts); same workspace. */
+tt_status tt_block_attn_ex(const tt_attn_desc *desc, const tt_attn_opts *opts, const void *q,
+                           const void *k_ctx, const void *v_ctx, const int32_t *ctx_lens,
+                           const void *k_blk, const void *v_blk, void *out, float *lse,
+                           void *workspace, size_t workspace_bytes, tt_stream_t stream);
+
+/*
+ * Combines two attention results over disjoint key sets (each with its natural-log
+ * lse) into the result over their union:
+ *   M = max(lse1, lse2), w_i = exp(lse_i - M) (0 where lse_i = -inf),
+ *   out = (w1 o1 + w2 o2) / (w1 + w2) (0 when both are -inf),
+ *   lse_out = M + log(w1 + w2) (-inf when both are), lse_out nullable.
+ * o1, o2, out: device bf16 [B, S, Hq, d] contiguous (16-byte aligned); lse1, lse2,
+ * lse_out: device fp32 [B, Hq, S].  out may alias o1 or o2; lse_out must not alias
+ * lse1 or lse2.
+ */
+tt_status tt_attn_lse_combine(int32_t B, int32_t S, int32_t Hq, int32_t d, const void *o1,
+                              const float *lse1, const void *o2, const float *lse2, void *out,
+                              float *lse_out, tt_stream_t stream);
+
+/*
  * Reads the device error word of an attention workspace into *flag_out (host).
  * It accumulates over every call that used the workspace since it was zeroed:
  * 0 = nothing to report; otherwise an OR of
  *   1  the TMA producer gave up on a wait,   2  an MMA issuer gave up on a wait,
  *   4  the softmax warps gave up on a wait,  8  a ctx_lens value was outside
- *      [0, Lmax] (that sequence was computed with the length clamped).
+ *      [0, Lmax] (that sequence was computed with the length clamped),
+ *   16 a paged cache's block table named a page outside the pool.
  * A wait that gives up leaves `out` incomplete.  Synchronizes `stream`.
  */
 tt_status tt_block_attn_error(const void *workspace, int32_t *flag_out, tt_stream_t stream);

@@ -1,3 +1,4 @@
 """fp64 CPU oracle -- test infrastructure only (tests, smoke check, bench CPU baseline)."""
-from .oracle import (block_attn, block_loop, build, confidence_unmask, generate_blocks,  # noqa: F401
-                     hw_threads, kv_append, load, mamba_state_seed)
+from .oracle import (adaln_single, bf16_decode, block_attn, block_loop, build,  # noqa: F401
+                     confidence_unmask, generate_blocks, hw_threads, kv_append, load, lse_combine,
+                     mamba_state_seed)

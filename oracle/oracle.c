@@ -99,20 +99,36 @@ static int run_parallel(item_fn fn, void *ctx, long n, int threads)
 
 /* ------------------------------------------------------------ attention */
 
+/* Which keys a block query sees: the prefix then the block (the one softmax of the
+ * two-tower mechanism), the context prefix alone, or the block alone (the aitrends.kr
+ * page names in-block self-attention and attention to the context separately). */
+enum { KEYS_ALL = 0, KEYS_PREFIX = 1, KEYS_BLOCK = 2 };
+
 struct attn_ctx {
     int B, S, Hq, Hkv, d, Lmax;
     double scale;
     const uint16_t *q, *k_ctx, *v_ctx, *k_blk, *v_blk;
+    const double *q64;  /* queries in fp64 (modulated), overrides q when given */
+    const double *gate; /* [B, Hq, d] output gate, or NULL */
     const int32_t *lens;
+    int keys;
     double *out, *lse;
 };
 
-/* Key j of the visible sequence for (b, kv head g): j < L_b is prefix row j of
- * the context-tower cache, j >= L_b is block row j - L_b. */
+/* Number of keys a query of sequence b sees. */
+static int visible(const struct attn_ctx *c, int b)
+{
+    int L = c->lens[b];
+    return c->keys == KEYS_PREFIX ? L : (c->keys == KEYS_BLOCK ? c->S : L + c->S);
+}
+
+/* Key j of the visible sequence for (b, kv head g): the prefix rows first (context
+ * tower cache row j), then the block rows (block row j - L_b); with only one of the
+ * two sets visible, its rows alone. */
 static const uint16_t *key_row(const struct attn_ctx *c, const uint16_t *ctx,
                                const uint16_t *blk, int b, int g, int j)
 {
-    int L = c->lens[b];
+    int L = c->keys == KEYS_BLOCK ? 0 : c->lens[b];
     if (j < L)
         return ctx + (((size_t)b * c->Hkv + g) * c->Lmax + j) * c->d;
     return blk + (((size_t)b * c->S + (j - L)) * c->Hkv + g) * c->d;
@@ -124,19 +140,27 @@ static void attn_item(void *p, long item)
     const struct attn_ctx *c = (const struct attn_ctx *)p;
     int b = (int)(item / c->Hq), h = (int)(item % c->Hq);
     int G = c->Hq / c->Hkv, g = h / G;          /* grouped-query head map */
-    int n = c->lens[b] + c->S;                  /* prefix keys, then block keys */
+    int n = visible(c, b);
     int d = c->d;
-    double *x = (double *)malloc(sizeof(double) * (size_t)n);
+    double *x = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
     double *acc = (double *)malloc(sizeof(double) * (size_t)d);
+    double *qd = (double *)malloc(sizeof(double) * (size_t)d);
 
     for (int s = 0; s < c->S; ++s) {
-        const uint16_t *qr = c->q + (((size_t)b * c->S + s) * c->Hq + h) * d;
+        size_t qi = (((size_t)b * c->S + s) * c->Hq + h) * d;
+        for (int e = 0; e < d; ++e) qd[e] = c->q64 ? c->q64[qi + e] : bf16_to_double(c->q[qi + e]);
+        double *o = c->out + qi;
+        if (n == 0) { /* no key: an empty sum */
+            for (int e = 0; e < d; ++e) o[e] = 0.0;
+            if (c->lse) c->lse[((size_t)b * c->Hq + h) * c->S + s] = -INFINITY;
+            continue;
+        }
         /* scores x_j = scale * <q, k_j> */
         double m = -INFINITY;
         for (int j = 0; j < n; ++j) {
             const uint16_t *kr = key_row(c, c->k_ctx, c->k_blk, b, g, j);
             double dot = 0.0;
-            for (int e = 0; e < d; ++e) dot += bf16_to_double(qr[e]) * bf16_to_double(kr[e]);
+            for (int e = 0; e < d; ++e) dot += qd[e] * bf16_to_double(kr[e]);
             x[j] = c->scale * dot;
             if (x[j] > m) m = x[j];
         }
@@ -149,12 +173,13 @@ static void attn_item(void *p, long item)
             const uint16_t *vr = key_row(c, c->v_ctx, c->v_blk, b, g, j);
             for (int e = 0; e < d; ++e) acc[e] += w * bf16_to_double(vr[e]);
         }
-        double *o = c->out + (((size_t)b * c->S + s) * c->Hq + h) * d;
-        for (int e = 0; e < d; ++e) o[e] = acc[e] / den;
+        const double *gt = c->gate ? c->gate + ((size_t)b * c->Hq + h) * d : NULL;
+        for (int e = 0; e < d; ++e) o[e] = (gt ? gt[e] : 1.0) * (acc[e] / den);
         if (c->lse) c->lse[((size_t)b * c->Hq + h) * c->S + s] = m + log(den);
     }
     free(x);
     free(acc);
+    free(qd);
 }
 
 /*
@@ -165,17 +190,41 @@ static void attn_item(void *p, long item)
  * [B,Hq,S], natural log.  Returns the number of threads used, or -1 on bad
  * arguments.  Context rows at or beyond L_b are never read.
  */
+int oracle_block_attn2(int B, int S, int Hq, int Hkv, int d, int Lmax, double scale,
+                       const uint16_t *q, const double *q64, const uint16_t *k_ctx,
+                       const uint16_t *v_ctx, const int32_t *ctx_lens, const uint16_t *k_blk,
+                       const uint16_t *v_blk, int keys, const double *gate, double *out,
+                       double *lse, int nthreads);
+
 int oracle_block_attn(int B, int S, int Hq, int Hkv, int d, int Lmax, double scale,
                       const uint16_t *q, const uint16_t *k_ctx, const uint16_t *v_ctx,
                       const int32_t *ctx_lens, const uint16_t *k_blk, const uint16_t *v_blk,
                       double *out, double *lse, int nthreads)
 {
+    return oracle_block_attn2(B, S, Hq, Hkv, d, Lmax, scale, q, NULL, k_ctx, v_ctx, ctx_lens,
+                              k_blk, v_blk, KEYS_ALL, NULL, out, lse, nthreads);
+}
+
+/*
+ * oracle_block_attn with the key set chosen (keys: 0 prefix then block, 1 prefix
+ * only, 2 block only; a row that sees no key gets out = 0 and lse = -inf), the
+ * queries optionally given in fp64 (q64 [B,S,Hq,d], e.g. modulated; then q is not
+ * read) and an optional output gate (gate [B,Hq,d] multiplies the result).
+ */
+int oracle_block_attn2(int B, int S, int Hq, int Hkv, int d, int Lmax, double scale,
+                       const uint16_t *q, const double *q64, const uint16_t *k_ctx,
+                       const uint16_t *v_ctx, const int32_t *ctx_lens, const uint16_t *k_blk,
+                       const uint16_t *v_blk, int keys, const double *gate, double *out,
+                       double *lse, int nthreads)
+{
+    if (keys < KEYS_ALL || keys > KEYS_BLOCK) return -1;
+    if (!q && !q64) return -1;
     if (B < 0 || S < 1 || Hq < 1 || Hkv < 1 || d < 1 || Lmax < 0 || Hq % Hkv != 0) return -1;
-    if (!q || !k_blk || !v_blk || !out || !ctx_lens || (Lmax > 0 && (!k_ctx || !v_ctx))) return -1;
+    if (!k_blk || !v_blk || !out || !ctx_lens || (Lmax > 0 && (!k_ctx || !v_ctx))) return -1;
     for (int b = 0; b < B; ++b)
         if (ctx_lens[b] < 0 || ctx_lens[b] > Lmax) return -1;
     struct attn_ctx c = {B, S, Hq, Hkv, d, Lmax, scale > 0.0 ? scale : 1.0 / sqrt((double)d),
-                         q, k_ctx, v_ctx, k_blk, v_blk, ctx_lens, out, lse};
+                         q, k_ctx, v_ctx, k_blk, v_blk, q64, gate, ctx_lens, keys, out, lse};
     long items = (long)B * Hq;
     return run_parallel(attn_item, &c, items, resolve_threads(nthreads, items));
 }

@@ -53,6 +53,9 @@ def load(path: Optional[str] = None):
     lib.oracle_block_attn.restype = _i
     lib.oracle_block_attn.argtypes = [_i, _i, _i, _i, _i, _i, ctypes.c_double,
                                       _p, _p, _p, _p, _p, _p, _p, _p, _i]
+    lib.oracle_block_attn2.restype = _i
+    lib.oracle_block_attn2.argtypes = [_i, _i, _i, _i, _i, _i, ctypes.c_double, _p, _p, _p, _p,
+                                       _p, _p, _p, _i, _p, _p, _p, _i]
     lib.oracle_confidence_unmask.restype = _i
     lib.oracle_confidence_unmask.argtypes = [_i, _i, _i, _i, _p, ctypes.c_double, ctypes.c_float,
                                              ctypes.c_int32, _i, _p, _p, _p, _p, _p, _p, _i]
@@ -73,13 +76,28 @@ def _c(a, dtype):
     return np.ascontiguousarray(a, dtype=dtype)
 
 
+KEYS = {"all": 0, "prefix": 1, "block": 2}
+
+
+def bf16_decode(bits) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> float64, exactly."""
+    u = np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return u.view(np.float32).astype(np.float64)
+
+
 def block_attn(q, k_ctx, v_ctx, ctx_lens, k_blk, v_blk, scale: float = 0.0,
-               nthreads: int = 0, lib=None, return_threads: bool = False):
+               nthreads: int = 0, lib=None, return_threads: bool = False, keys: str = "all",
+               q_scale=None, q_shift=None, o_gate=None):
     """Exact block-query attention in fp64.
 
     q [B,S,Hq,d], k_ctx/v_ctx [B,Hkv,Lmax,d], k_blk/v_blk [B,S,Hkv,d]: bf16 bit
     patterns (uint16).  ctx_lens int32[B].  scale <= 0 means 1/sqrt(d).
-    Returns (out float64 [B,S,Hq,d], lse float64 [B,Hq,S]).
+    keys: "all" (the prefix then the block, one softmax), "prefix" or "block" (one of
+    the two key sets alone; a row that sees no key gets out 0 and lse -inf).
+    q_scale, q_shift, o_gate ([B,Hq,d], optional): adaLN-single modulation, in fp64:
+    queries q * (1 + q_scale) + q_shift, output multiplied by o_gate (the aitrends.kr
+    page, technical features: scale, shift and gate per timestep in each denoiser
+    layer).  Returns (out float64 [B,S,Hq,d], lse float64 [B,Hq,S]).
     """
     lib = lib or load()
     q, k_blk, v_blk = _c(q, np.uint16), _c(k_blk, np.uint16), _c(v_blk, np.uint16)
@@ -89,12 +107,70 @@ def block_attn(q, k_ctx, v_ctx, ctx_lens, k_blk, v_blk, scale: float = 0.0,
     Hkv, Lmax = k_ctx.shape[1], k_ctx.shape[2]
     out = np.empty((B, S, Hq, d), dtype=np.float64)
     lse = np.empty((B, Hq, S), dtype=np.float64)
-    used = lib.oracle_block_attn(B, S, Hq, Hkv, d, Lmax, float(scale), _ptr(q), _ptr(k_ctx),
-                                 _ptr(v_ctx), _ptr(lens), _ptr(k_blk), _ptr(v_blk), _ptr(out),
-                                 _ptr(lse), int(nthreads))
+    q64 = None
+    if q_scale is not None or q_shift is not None:
+        sc = np.zeros((B, Hq, d)) if q_scale is None else np.asarray(q_scale, np.float64)
+        sh = np.zeros((B, Hq, d)) if q_shift is None else np.asarray(q_shift, np.float64)
+        q64 = _c(bf16_decode(q) * (1.0 + sc[:, None]) + sh[:, None], np.float64)
+    gate = None if o_gate is None else _c(o_gate, np.float64)
+    used = lib.oracle_block_attn2(B, S, Hq, Hkv, d, Lmax, float(scale), _ptr(q), _ptr(q64),
+                                  _ptr(k_ctx), _ptr(v_ctx), _ptr(lens), _ptr(k_blk), _ptr(v_blk),
+                                  KEYS[keys], _ptr(gate), _ptr(out), _ptr(lse), int(nthreads))
     if used < 0:
-        raise ValueError("oracle_block_attn: invalid arguments")
+        raise ValueError("oracle_block_attn2: invalid arguments")
     return (out, lse, used) if return_threads else (out, lse)
+
+
+def lse_combine(o1, lse1, o2, lse2):
+    """The softmax over the union of two disjoint key sets from the results over each
+    (o [B,S,Hq,d], natural-log lse [B,Hq,S], float64): with M = max(lse1, lse2) and
+    w_i = exp(lse_i - M), o = (w1 o1 + w2 o2) / (w1 + w2), lse = M + log(w1 + w2); a
+    side with lse = -inf (no key) weighs nothing, and both gives o = 0, lse = -inf."""
+    l1 = np.asarray(lse1, np.float64)
+    l2 = np.asarray(lse2, np.float64)
+    M = np.maximum(l1, l2)
+    finite = np.isfinite(M)
+    Ms = np.where(finite, M, 0.0)
+    w1 = np.where(np.isfinite(l1), np.exp(np.where(np.isfinite(l1), l1, 0.0) - Ms), 0.0)
+    w2 = np.where(np.isfinite(l2), np.exp(np.where(np.isfinite(l2), l2, 0.0) - Ms), 0.0)
+    den = w1 + w2
+    # [B,Hq,S] weights onto [B,S,Hq,1]
+    t = lambda x: np.transpose(x, (0, 2, 1))[..., None]  # noqa: E731
+    with np.errstate(invalid="ignore", divide="ignore"):
+        o = np.where(t(den) > 0, (t(w1) * o1 + t(w2) * o2) / np.where(t(den) > 0, t(den), 1.0), 0.0)
+        lse = np.where(den > 0, Ms + np.log(np.where(den > 0, den, 1.0)), -np.inf)
+    return o, lse
+
+
+def adaln_single(t, w1, b1, w2, b2, embed, layer: int):
+    """adaLN-single modulation of one denoiser layer from the diffusion timestep.
+
+    The pages say each denoiser layer is modulated by the diffusion timestep through
+    adaLN-single, which injects a scale, shift and gate per timestep with about 1.5 M
+    added parameters (aitrends.kr, "Nemotron-Labs-TwoTower-30B-A3B-Base-BF16", section
+    기술적 특징; dothoosh.com, architecture bullets).  adaLN-single computes the
+    modulation once from the timestep with a small network shared by all layers and
+    adds a per-layer learned offset.  Reading (the pages give no further detail):
+      e(t)  = [cos(t w_0), .., cos(t w_{F/2-1}), sin(t w_0), .., sin(t w_{F/2-1})],
+              w_i = 10000^(-i / (F/2))   (a sinusoidal timestep embedding of size F);
+      h     = SiLU(W1 e(t) + b1),  SiLU(x) = x / (1 + exp(-x))   (W1 [Dh, F]);
+      m     = W2 h + b2 + embed[layer]   (W2 [3 N, Dh], embed [layers, 3 N]);
+      shift, scale, gate = m[0:N], m[N:2N], m[2N:3N].
+    t: [B] float timesteps.  Returns (shift, scale, gate), each float64 [B, N].
+    """
+    t = np.asarray(t, np.float64)
+    w1 = np.asarray(w1, np.float64)
+    F = w1.shape[1]
+    half = F // 2
+    freqs = 10000.0 ** (-np.arange(half, dtype=np.float64) / half)
+    arg = t[:, None] * freqs[None, :]
+    e = np.concatenate([np.cos(arg), np.sin(arg)], axis=1)
+    pre = e @ w1.T + np.asarray(b1, np.float64)[None, :]
+    h = pre / (1.0 + np.exp(-pre))
+    m = h @ np.asarray(w2, np.float64).T + np.asarray(b2, np.float64)[None, :] + \
+        np.asarray(embed, np.float64)[layer][None, :]
+    N = m.shape[1] // 3
+    return m[:, :N], m[:, N:2 * N], m[:, 2 * N:]
 
 
 def confidence_unmask(logits, dtype: str, temperature: float, threshold: float,

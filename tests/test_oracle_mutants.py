@@ -23,10 +23,11 @@ MUTANTS = [
     ("dropped_scale", "x[j] = c->scale * dot;", "x[j] = dot;"),
     ("value_uses_key", "const uint16_t *vr = key_row(c, c->v_ctx, c->v_blk, b, g, j);",
      "const uint16_t *vr = key_row(c, c->k_ctx, c->k_blk, b, g, j);"),
-    ("dropped_block_keys", "int n = c->lens[b] + c->S;", "int n = c->lens[b] + 1;"),
-    ("q_layout_transposed", "const uint16_t *qr = c->q + (((size_t)b * c->S + s) * c->Hq + h) * d;",
-     "const uint16_t *qr = c->q + (((size_t)b * c->Hq + h) * c->S + s) * d;"),
-    ("dropped_normaliser", "o[e] = acc[e] / den;", "o[e] = acc[e];"),
+    ("dropped_block_keys", "(c->keys == KEYS_BLOCK ? c->S : L + c->S)",
+     "(c->keys == KEYS_BLOCK ? c->S : L + 1)"),
+    ("q_layout_transposed", "bf16_to_double(c->q[qi + e])",
+     "bf16_to_double(c->q[(((size_t)b * c->Hq + h) * c->S + s) * d + e])"),
+    ("dropped_normaliser", "* (acc[e] / den);", "* (acc[e]);"),
     ("temperature_multiplies", "- best) / c->temperature);", "- best) * c->temperature);"),
     ("argmax_last_tie", "if (l > best) { best = l; arg = v; }", "if (l >= best) { best = l; arg = v; }"),
     ("threshold_strict", "if (force_commit_all || cf >= threshold) {",
