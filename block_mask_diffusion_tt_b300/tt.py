@@ -50,6 +50,11 @@ class AttnOpts(ctypes.Structure):
                 ("q_scale", _p), ("q_shift", _p), ("o_gate", _p)]
 
 
+class AdalnDesc(ctypes.Structure):
+    _fields_ = [("B", _i32), ("F", _i32), ("Dh", _i32), ("N", _i32), ("layer", _i32),
+                ("n_layers", _i32)]
+
+
 class UnmaskDesc(ctypes.Structure):
     _fields_ = [("B", _i32), ("S", _i32), ("V", _i32), ("logits_dtype", ctypes.c_int),
                 ("logits_row_stride", ctypes.c_int64), ("temperature", ctypes.c_float),
@@ -109,6 +114,8 @@ def load(path: str = LIB_PATH):
                                             _p, _p, _p, _p, _p, _p, _p, _p, _sz, _p]),
         "tt_attn_lse_combine": (ctypes.c_int, [_i32, _i32, _i32, _i32, _p, _p, _p, _p, _p, _p,
                                                _p]),
+        "tt_adaln_single": (ctypes.c_int, [ctypes.POINTER(AdalnDesc), _p, _p, _p, _p, _p, _p, _p,
+                                           _p, _p, _p]),
         "tt_confidence_unmask_workspace_size": (_sz, [ctypes.POINTER(UnmaskDesc)]),
         "tt_confidence_unmask": (ctypes.c_int, [ctypes.POINTER(UnmaskDesc), _p, _p, _p, _p, _p, _p,
                                                 _i32, _p, _sz, _p]),
@@ -283,6 +290,25 @@ def attn_lse_combine(o1, lse1, o2, lse2, out=None, lse_out=None, stream=None):
     check(load().tt_attn_lse_combine(B, S, Hq, d, _ptr(o1), _ptr(lse1), _ptr(o2), _ptr(lse2),
                                      _ptr(out), _ptr(lse_out), _stream(stream)))
     return out
+
+
+def adaln_single(t, w1, b1, w2, b2, embed, layer: int, stream=None):
+    """adaLN-single shift, scale and gate of one layer (tt_adaln_single); fp32 tensors.
+
+    t [B]; w1 [Dh, F]; b1 [Dh]; w2 [3N, Dh]; b2 [3N]; embed [layers, 3N].
+    Returns (shift, scale, gate), each [B, N].
+    """
+    for x, n in ((t, "t"), (w1, "w1"), (b1, "b1"), (w2, "w2"), (b2, "b2"), (embed, "embed")):
+        _need(x, n, torch.float32)
+        if not x.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    B, (Dh, F), N = t.shape[0], w1.shape, w2.shape[0] // 3
+    outs = [torch.empty((B, N), dtype=torch.float32, device=t.device) for _ in range(3)]
+    desc = AdalnDesc(B=B, F=F, Dh=Dh, N=N, layer=int(layer), n_layers=embed.shape[0])
+    check(load().tt_adaln_single(ctypes.byref(desc), _ptr(t), _ptr(w1), _ptr(b1), _ptr(w2),
+                                 _ptr(b2), _ptr(embed), _ptr(outs[0]), _ptr(outs[1]),
+                                 _ptr(outs[2]), _stream(stream)))
+    return tuple(outs)
 
 
 def block_attn_noalloc(q, k_ctx, v_ctx, ctx_lens, k_blk, v_blk, out=None, lse=None,
@@ -600,4 +626,4 @@ def exported_symbols() -> list:
             "tt_denoise_block_loop",
             "tt_synth_logits", "tt_synth_logits_producer", "tt_kv_append",
             "tt_mamba_state_seed", "tt_generate_blocks_workspace_size", "tt_generate_blocks",
-            "tt_block_attn_ex", "tt_attn_lse_combine"]
+            "tt_block_attn_ex", "tt_attn_lse_combine", "tt_adaln_single"]

@@ -443,6 +443,35 @@ tt_status tt_kv_append(const tt_kv_desc *desc, void *const *k_ctx, void *const *
                        int32_t *ctx_lens, const void *const *k_blk, const void *const *v_blk,
                        const uint8_t *active, int32_t *overflow, tt_stream_t stream);
 
+/* ------------------------------------------------------------- adaLN-single
+ *
+ * Time conditioning of the denoiser: every denoiser layer gets a scale, shift and
+ * gate per diffusion timestep from an adaLN-single module (aitrends.kr,
+ * "Nemotron-Labs-TwoTower-30B-A3B-Base-BF16", section "technical features": about
+ * 1.5 M added parameters; dothoosh.com, architecture bullets).  tt_adaln_single
+ * computes them; tt_block_attn_ex applies them to the attention (tt_attn_opts).
+ */
+typedef struct {
+    int32_t B;        /* sequences */
+    int32_t F;        /* timestep embedding size, even, <= 1024 */
+    int32_t Dh;       /* hidden size of the shared network, <= 512 */
+    int32_t N;        /* size of each modulation vector (Hq*d for the attention) */
+    int32_t layer;    /* which row of `embed` */
+    int32_t n_layers; /* rows of `embed` */
+} tt_adaln_desc;
+
+/*
+ * For every sequence b with timestep t[b] (device fp32 [B]):
+ *   e = [cos(t w_i)]_{i<F/2} ++ [sin(t w_i)]_{i<F/2},  w_i = 10000^(-i/(F/2));
+ *   h = SiLU(W1 e + b1);  m = W2 h + b2 + embed[layer];
+ *   shift[b] = m[0:N], scale[b] = m[N:2N], gate[b] = m[2N:3N].
+ * Device fp32 arrays: w1 [Dh, F], b1 [Dh], w2 [3N, Dh], b2 [3N], embed [n_layers, 3N],
+ * outputs shift, scale, gate [B, N].  One launch.
+ */
+tt_status tt_adaln_single(const tt_adaln_desc *desc, const float *t, const float *w1,
+                          const float *b1, const float *w2, const float *b2, const float *embed,
+                          float *shift, float *scale, float *gate, tt_stream_t stream);
+
 /* ---------------------------------------------------------- Mamba-2 state seeding
  *
  * The denoiser's Mamba-2 layers start from the context tower's states: each
