@@ -5,6 +5,8 @@ the log-sum-exp.  Small cases are compared element by element over every output;
 the full-size workloads run in the launch configuration the bench times and are
 compared on sampled sequences (all heads and block rows of each).
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -116,6 +118,36 @@ def test_lse_optional_and_workspace_reuse():
         _gpu.assert_attn_close(out.float().cpu().numpy().astype(np.float64), ref, what="reuse")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_workspace_reuse_across_split_patterns(d):
+    """One workspace serves calls whose lengths split the pairs across CTAs in
+    different ways (two CTAs, a few, every SM): each result is bit for bit that of a
+    fresh workspace, and no error is flagged."""
+    B, Lmax = 4, 40000
+    cases = [[40000, 0, 0, 0], [3000, 1200, 64, 2999], [20000, 20000, 100, 5],
+             [40000, 39999, 1, 0], [700, 650, 600, 550], [40000, 0, 0, 0]]
+    shape = synth.AttnShape(B, 16, 32, 2, d, Lmax, lens=cases[0])
+    inp = synth.attn_inputs(shape, seed=21 + d)
+    dd = _gpu.attn_dev(inp)
+    desc = tt.attn_desc(dd["q"], dd["k_ctx"], dd["v_ctx"], dd["k_blk"], dd["v_blk"], dd["q"])
+    ws = tt.Workspace(tt.block_attn_workspace_size(desc))
+    for lens in cases:
+        lt = torch.tensor(lens, dtype=torch.int32, device=_gpu.DEV)
+        got = tt.block_attn(dd["q"], dd["k_ctx"], dd["v_ctx"], lt, dd["k_blk"], dd["v_blk"],
+                            workspace=ws)
+        fresh = tt.block_attn(dd["q"], dd["k_ctx"], dd["v_ctx"], lt, dd["k_blk"], dd["v_blk"],
+                              workspace=tt.Workspace(tt.block_attn_workspace_size(desc)))
+        torch.cuda.synchronize()
+        assert torch.equal(got.view(torch.int16), fresh.view(torch.int16)), lens
+        flag = ctypes.c_int32(-1)
+        tt.check(tt.load().tt_block_attn_error(ws.ptr, ctypes.byref(flag), None))
+        assert flag.value == 0, lens
+    # the last case against the oracle too
+    ref, _ = oracle.block_attn(inp["q"], inp["k_ctx"], inp["v_ctx"], np.asarray(cases[-1]),
+                               inp["k_blk"], inp["v_blk"])
+    _gpu.assert_attn_close(got.float().cpu().numpy().astype(np.float64), ref, what="reuse")
+
+
 def test_empty_batch():
     z = torch.zeros((0, 16, 8, 128), dtype=torch.bfloat16, device=_gpu.DEV)
     kv = torch.zeros((0, 2, 10, 128), dtype=torch.bfloat16, device=_gpu.DEV)
@@ -155,7 +187,6 @@ def test_out_of_range_lengths_are_reported_and_clamped():
     """ctx_lens lives on the device, so the host cannot validate it: a length below 0 or
     above Lmax sets flag 8 of the workspace error word, and that sequence is computed
     with its length clamped into [0, Lmax].  A call with valid lengths leaves the word 0."""
-    import ctypes
     shape = synth.AttnShape(3, 16, 8, 2, 128, 200, lens=[0, 77, 200])
     inp = synth.attn_inputs(shape, seed=31)
     d = _gpu.attn_dev(inp)
