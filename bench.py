@@ -626,6 +626,49 @@ def run_reference(args, dist: Dist) -> dict:
         gpu_launches=0)
 
 
+def h2d_pinned_gbs(nbytes: int = 256 << 20, reps: int = 5) -> float:
+    """Host-to-device copy rate from pinned memory (the link the e2e number crosses)."""
+    host = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    dev = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    dev.copy_(host, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        dev.copy_(host, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    return reps * nbytes / (e0.elapsed_time(e1) * 1e-3) / 1e9
+
+
+def run_extras(args) -> dict:
+    """Measurements of the other entry points, taken after the timed region (CUDA
+    events around each call): the block loop over the sweep configuration (every S
+    and gamma), block-by-block generation, Mamba-2 state seeding, the K/V append, and
+    the host link's pinned copy rate."""
+    from block_mask_diffusion_tt_b300 import profile
+    ws = synth.workloads()
+    w = ws[args.workload]
+    peak = measured_peaks()["hbm_gbs"]
+    out = {}
+    sw = ws["sweep"]
+    _, recs, _ = profile.run_loop(sw, 2, True)
+    out["sweep"] = dict(workload=f"sweep B={sw.attn.B} V={sw.V} steps=S spike p 0.2->0.9 "
+                                 f"T={sw.temperature}",
+                        blocks=recs)
+    _, gen, _ = profile.run_generate(w, 4, True)
+    out["generate"] = dict(workload=w.name, max_new_tokens=4 * w.attn.S, **gen)
+    us, gbs, how = profile.run_seed(w, 20, True)
+    out["mamba_state_seed"] = dict(workload=f"{w.name} B={w.attn.B}, {how}", us=us, hbm_gbs=gbs,
+                                   frac_of_measured=gbs / peak)
+    us, gbs, how = profile.run_kvappend(w, 20, True)
+    out["kv_append"] = dict(workload=f"{w.name}, {how}", us=us, hbm_gbs=gbs,
+                            frac_of_measured=gbs / peak)
+    out["h2d_pinned_gbs"] = h2d_pinned_gbs()
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -634,6 +677,8 @@ def main():
     ap.add_argument("--workload", default="ragged16k", choices=sorted(synth.workloads()))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the measurements of the other entry points (1 GPU only)")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     args = ap.parse_args()
     if args.warmup < 3:
@@ -645,6 +690,8 @@ def main():
                 print(json.dumps(run_reference(args, dist)), flush=True)
             return
         res = run_ours(args, dist)
+        if dist.world == 1 and not args.no_extras:
+            res["extras"] = run_extras(args)
         if dist.rank == 0:
             if dist.world == 1:
                 res["cpu_baseline"] = cpu_baseline(synth.workloads()[args.workload],

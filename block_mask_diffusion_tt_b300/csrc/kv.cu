@@ -6,18 +6,21 @@
 // prefix.  Here the block's K/V rows of each layer are copied into rows
 // [L_b, L_b + S) of that layer's cache and the prefix length grows by S.
 //
-// One CTA per sequence b: it reads L_b once, copies every layer's K and V rows as
-// 16-byte vectors (coalesced on both sides: a row is d contiguous elements), with
-// kKvUnroll loads in flight per thread before their stores, then writes L_b + S.
-// Only CTA b touches ctx_lens[b], so one launch needs no ordering between CTAs.  A sequence that is not active, or whose block would not fit under
-// Lmax, is left as it is; the second case is counted in a device word.
+// Two launches.  The copy: one CTA per (layer, K or V, sequence) moves that
+// block's S x Hkv rows as 16-byte vectors (coalesced on both sides: a row is d
+// contiguous elements), kKvUnroll loads in flight per thread before their stores,
+// to rows [L_b, L_b + S).  Then one small CTA advances every length taking part;
+// stream order puts it after all copies, which read the old lengths.  A sequence
+// that is not active, or whose block would not fit under Lmax, is left as it is;
+// the second case is counted in a device word.
 #include "common.cuh"
 
 namespace tt {
 namespace {
 
-constexpr int kKvThreads = 1024;
+constexpr int kKvThreads = 256;
 constexpr int kKvUnroll = 4;
+constexpr int kLenThreads = 256;
 
 struct KvArgs {
     const uint16_t *kb[TT_KV_MAX_LAYERS];
@@ -25,29 +28,26 @@ struct KvArgs {
     uint16_t *kc[TT_KV_MAX_LAYERS];
     uint16_t *vc[TT_KV_MAX_LAYERS];
     int64_t cs[3], bs[3];  // cache [B, Hkv, Lmax, d] and block [B, S, Hkv, d] strides
-    int S, Hkv, d, Lmax, nl;
+    int B, S, Hkv, d, Lmax, nl;
     int32_t *lens;
     const uint8_t *active;
     int32_t *overflow;
 };
 
-__global__ void __launch_bounds__(kKvThreads) kv_append_kernel(const KvArgs a) {
-    const int b = blockIdx.x;
-    __shared__ int s_len, s_go;
-    if (threadIdx.x == 0) {
-        const int L = a.lens[b];
-        const bool act = a.active == nullptr || a.active[b] != 0;
-        const bool fits = L >= 0 && static_cast<int64_t>(L) + a.S <= a.Lmax;
-        if (act && !fits && a.overflow) atomicAdd(a.overflow, 1);
-        s_len = L;
-        s_go = act && fits;
-    }
-    __syncthreads();
-    if (!s_go) return;
-    const int L = s_len;
+__device__ __forceinline__ bool takes_part(const KvArgs &a, int b, int L) {
+    const bool act = a.active == nullptr || a.active[b] != 0;
+    return act && L >= 0 && static_cast<int64_t>(L) + a.S <= a.Lmax;
+}
+
+// blockIdx.x = layer * 2 + (0: K, 1: V), blockIdx.y = sequence
+__global__ void __launch_bounds__(kKvThreads) kv_copy_kernel(const KvArgs a) {
+    const int b = blockIdx.y, l = blockIdx.x >> 1, kv = blockIdx.x & 1;
+    const int L = a.lens[b];
+    if (!takes_part(a, b, L)) return;
     const int vpr = a.d / 8;  // 16-byte vectors per row
-    const int per_kv = a.S * a.Hkv * vpr;
-    const int total = a.nl * 2 * per_kv;
+    const int total = a.S * a.Hkv * vpr;
+    const uint16_t *sb = (kv ? a.vb[l] : a.kb[l]) + b * a.bs[0];
+    uint16_t *db = (kv ? a.vc[l] : a.kc[l]) + b * a.cs[0];
     for (int i0 = threadIdx.x; i0 < total; i0 += kKvUnroll * kKvThreads) {
         uint4 val[kKvUnroll];
         uint16_t *dst[kKvUnroll];
@@ -56,17 +56,11 @@ __global__ void __launch_bounds__(kKvThreads) kv_append_kernel(const KvArgs a) {
             const int i = i0 + u * kKvThreads;
             dst[u] = nullptr;
             if (i < total) {
-                const int l = i / (2 * per_kv);
-                const int r = i - l * 2 * per_kv;
-                const int kv = r / per_kv;
-                const int r2 = r - kv * per_kv;
-                const int s = r2 / (a.Hkv * vpr);
-                const int g = (r2 / vpr) % a.Hkv;
-                const int v = r2 % vpr;
-                const uint16_t *src =
-                    (kv ? a.vb[l] : a.kb[l]) + b * a.bs[0] + s * a.bs[1] + g * a.bs[2] + 8 * v;
-                dst[u] = (kv ? a.vc[l] : a.kc[l]) + b * a.cs[0] + g * a.cs[1] +
-                         static_cast<int64_t>(L + s) * a.cs[2] + 8 * v;
+                const int s = i / (a.Hkv * vpr);
+                const int g = (i / vpr) % a.Hkv;
+                const int v = i % vpr;
+                const uint16_t *src = sb + s * a.bs[1] + g * a.bs[2] + 8 * v;
+                dst[u] = db + g * a.cs[1] + static_cast<int64_t>(L + s) * a.cs[2] + 8 * v;
                 val[u] = __ldcs(reinterpret_cast<const uint4 *>(src));
             }
         }
@@ -74,13 +68,22 @@ __global__ void __launch_bounds__(kKvThreads) kv_append_kernel(const KvArgs a) {
         for (int u = 0; u < kKvUnroll; ++u)
             if (dst[u]) *reinterpret_cast<uint4 *>(dst[u]) = val[u];
     }
-    __syncthreads();
-    if (threadIdx.x == 0) a.lens[b] = L + a.S;
+}
+
+__global__ void __launch_bounds__(kLenThreads) kv_len_kernel(const KvArgs a) {
+    for (int b = threadIdx.x; b < a.B; b += kLenThreads) {
+        const int L = a.lens[b];
+        if (takes_part(a, b, L)) {
+            a.lens[b] = L + a.S;
+        } else if ((a.active == nullptr || a.active[b] != 0) && a.overflow) {
+            atomicAdd(a.overflow, 1);
+        }
+    }
 }
 
 tt_status validate_kv(const tt_kv_desc *d, const char *fn) {
     if (!d) return fail(TT_ERR_INVALID_ARG, "%s: null desc", fn);
-    if (d->B < 0 || d->S < 1 || d->Hkv < 1 || d->Lmax < 0)
+    if (d->B < 0 || d->B > 65535 || d->S < 1 || d->Hkv < 1 || d->Lmax < 0)
         return fail(TT_ERR_INVALID_ARG, "%s: bad shape B=%d S=%d Hkv=%d Lmax=%d", fn, d->B, d->S,
                     d->Hkv, d->Lmax);
     if (d->d < 8 || d->d > 512 || d->d % 8 != 0)
@@ -141,9 +144,14 @@ extern "C" tt_status tt_kv_append(const tt_kv_desc *desc, void *const *k_ctx, vo
     a.d = desc->d;
     a.Lmax = desc->Lmax;
     a.nl = desc->n_layers;
+    a.B = desc->B;
     a.lens = ctx_lens;
     a.active = active;
     a.overflow = overflow;
-    kv_append_kernel<<<desc->B, kKvThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
-    return cuda_status(cudaGetLastError(), "tt_kv_append launch");
+    const cudaStream_t st_ = static_cast<cudaStream_t>(stream);
+    kv_copy_kernel<<<dim3(2 * desc->n_layers, desc->B), kKvThreads, 0, st_>>>(a);
+    tt_status s2 = cuda_status(cudaGetLastError(), "tt_kv_append copy launch");
+    if (s2 != TT_OK) return s2;
+    kv_len_kernel<<<1, kLenThreads, 0, st_>>>(a);
+    return cuda_status(cudaGetLastError(), "tt_kv_append length launch");
 }

@@ -132,12 +132,13 @@ def run_unmask(w: synth.Workload, n: int, time_it: bool = False):
 
 def run_loop(w: synth.Workload, n: int, time_it: bool = False):
     """One block per (S, gamma) of the workload's sweep (or its own S and gamma),
-    n times each; with time_it, the mean time of a block and what it committed."""
+    n times each; with time_it, the mean time of a block and what it committed (as
+    text lines and as one record per (S, gamma))."""
     a = w.attn
     ex = w.extra or {}
     s_values = ex.get("S_values", (a.S,))
     gammas = ex.get("gammas", (w.threshold,))
-    lines = []
+    lines, records = [], []
     for S in s_values:
         ps = [synth.sweep_spike_p(k, S, ex.get("spike_p_first", w.spike_p),
                                   ex.get("spike_p_last", w.spike_p)) for k in range(S)]
@@ -168,7 +169,10 @@ def run_loop(w: synth.Workload, n: int, time_it: bool = False):
                 lines.append(f"S={S:2d} gamma={gamma:.2f}: {us:8.1f} us per block, "
                              f"{a.B * S / us * 1e6:12.0f} committed tokens/s, "
                              f"steps used per block {mean_used:.2f} (loop ran {steps})")
-    return ("\n".join(lines), None, None) if time_it else None
+                records.append(dict(S=S, gamma=gamma, us_per_block=us,
+                                    committed_tokens_per_s=a.B * S / us * 1e6,
+                                    steps_per_block=mean_used))
+    return ("\n".join(lines), records, None) if time_it else None
 
 
 def run_kvappend(w: synth.Workload, n: int, time_it: bool = False):
@@ -305,7 +309,9 @@ def run_generate(w: synth.Workload, n: int, time_it: bool = False):
     toks = int(gen_len.sum())
     mean_steps = float(steps.float().mean()) / max(blocks, 1)
     return (f"{blocks} blocks, {toks} tokens in {us / 1e3:.2f} ms: {toks / us * 1e6:.0f} "
-            f"generated tokens/s, {mean_steps:.2f} steps per block", None, None)
+            f"generated tokens/s, {mean_steps:.2f} steps per block",
+            dict(blocks=blocks, tokens=toks, ms=us / 1e3, generated_tokens_per_s=toks / us * 1e6,
+                 steps_per_block=mean_steps), None)
 
 
 def main():

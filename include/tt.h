@@ -436,8 +436,9 @@ typedef struct {
  *                 takes part but has L_b < 0 or L_b + S > Lmax; such a sequence's
  *                 cache and length are left unchanged.
  * Strides are in elements, positive multiples of 8 with the innermost one 1, and
- * every pointer 16-byte aligned; d is a multiple of 8 up to 512.  One launch; the
- * call returns once it is enqueued.
+ * every pointer 16-byte aligned; d is a multiple of 8 up to 512; B <= 65535.  Two
+ * launches on `stream` (the copies, then the length update); the call returns once
+ * they are enqueued.
  */
 tt_status tt_kv_append(const tt_kv_desc *desc, void *const *k_ctx, void *const *v_ctx,
                        int32_t *ctx_lens, const void *const *k_blk, const void *const *v_blk,
