@@ -48,7 +48,27 @@ def attn_bytes(a, lens_np) -> int:
     return kv + a.B * a.S * a.Hkv * a.d * 2 * 2 + a.B * a.S * a.Hq * a.d * 2 * 2
 
 
-def run_attn(w: synth.Workload, n: int, time_it: bool = False):
+def _graph_us(fn, n: int) -> float:
+    """Device time per call of fn(i) for i < n: the n calls are captured in one CUDA
+    graph and its replay is timed with CUDA events, so the host's launch cost does
+    not enter (a small call enqueues in about as long as it runs)."""
+    fn(0)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for i in range(n):
+            fn(i)
+    graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / n
+
+
+def run_attn(w: synth.Workload, n: int, time_it: bool = False, graph: bool = False):
     a = w.attn
     g = torch.Generator(device="cuda")
     g.manual_seed(w.seed)
@@ -76,6 +96,13 @@ def run_attn(w: synth.Workload, n: int, time_it: bool = False):
     def call(i):
         tt.check(lib.tt_block_attn(*argv[i]))
 
+    if graph:
+        def gcall(i):  # on the stream being captured
+            cs = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+            tt.check(lib.tt_block_attn(*(argv[i % nl][:-1] + (cs,))))
+
+        us = _graph_us(gcall, max(n, nl))
+        return us, attn_bytes(a, lens_np) / us / 1e3, f"{nl} layers, one CUDA graph"
     for _ in range(3):
         for i in range(nl):
             call(i)
@@ -92,7 +119,7 @@ def run_attn(w: synth.Workload, n: int, time_it: bool = False):
     return us, attn_bytes(a, lens_np) / us / 1e3, f"{nl} layers"
 
 
-def run_unmask(w: synth.Workload, n: int, time_it: bool = False):
+def run_unmask(w: synth.Workload, n: int, time_it: bool = False, graph: bool = False):
     a = w.attn
     logits = tt.synth_logits(w.seed, 0, a.B, a.S, w.V, w.sigma,
                              synth.spike_threshold(w.spike_p), tt.TT_BF16)
@@ -114,6 +141,19 @@ def run_unmask(w: synth.Workload, n: int, time_it: bool = False):
     init_args = (ctypes.byref(desc), tt._ptr(tokens), tt._ptr(masked), None, None, sp)
     unmask_args = (ctypes.byref(desc), tt._ptr(logits), tt._ptr(tokens), tt._ptr(masked),
                    tt._ptr(conf), tt._ptr(now), tt._ptr(remaining), 0, ws.ptr, ws.nbytes, sp)
+    nbytes = a.B * a.S * w.V * 2 + a.B * a.S * (4 + 1 + 4 + 1 + 4) + a.B * 4
+    if graph:
+        def both(i):
+            cs = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+            tt.check(lib.tt_block_init(*(init_args[:-1] + (cs,))))
+            tt.check(lib.tt_confidence_unmask(*(unmask_args[:-1] + (cs,))))
+
+        def init_only(i):
+            cs = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+            tt.check(lib.tt_block_init(*(init_args[:-1] + (cs,))))
+
+        us = _graph_us(both, n) - _graph_us(init_only, n)
+        return us, nbytes / us / 1e3, "one CUDA graph, block init subtracted"
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(n)]
     for i in range(3 + n):
@@ -126,7 +166,6 @@ def run_unmask(w: synth.Workload, n: int, time_it: bool = False):
     torch.cuda.synchronize()
     us = sum(s.elapsed_time(e) for s, e in ev) * 1e3 / n
     # every position is masked at a block's first step: whole rows plus the state arrays
-    nbytes = a.B * a.S * w.V * 2 + a.B * a.S * (4 + 1 + 4 + 1 + 4) + a.B * 4
     return us, nbytes / us / 1e3, "events around each call"
 
 
@@ -321,12 +360,15 @@ def main():
     ap.add_argument("n", type=int, nargs="?", default=4)
     ap.add_argument("--time", action="store_true",
                     help="time n back-to-back calls with CUDA events instead")
+    ap.add_argument("--graph", action="store_true",
+                    help="with --time (attn, unmask): time a CUDA-graph replay of the n calls")
     args = ap.parse_args()
     tt.load()
     w = synth.workloads()[args.workload]
     run = dict(attn=run_attn, unmask=run_unmask, loop=run_loop, kvappend=run_kvappend,
                seed=run_seed, generate=run_generate)[args.op]
-    res = run(w, args.n, args.time)
+    res = run(w, args.n, args.time, args.graph) if args.op in ("attn", "unmask") else \
+        run(w, args.n, args.time)
     torch.cuda.synchronize()
     if res is None:
         print("ok", args.op, w.name, args.n)
