@@ -326,21 +326,22 @@ class DeviceWorkload:
         return a.B * a.S * self.w.V * 2 + a.B * a.S * (4 + 1 + 4 + 1 + 4) + a.B * 4
 
     def step(self, stream, ev_attn=None, ev_unmask=None):
-        """Enqueues one denoiser step; optional event pairs bracket the kernels."""
+        """Enqueues one denoiser step; optional event pairs bracket the attention calls
+        (one pair around the layers' back-to-back calls) and the unmask call."""
         sp = ctypes.c_void_p(stream.cuda_stream)
         lib = self.lib
         tt.check(lib.tt_block_init(ctypes.byref(self.unmask_desc), tt._ptr(self.tokens),
                                    tt._ptr(self.masked), None, None, sp))
         for i, ly in enumerate(self.layers):
-            if ev_attn is not None:
-                ev_attn[i][0].record(stream)
+            if ev_attn is not None and i == 0:
+                ev_attn[0].record(stream)
             tt.check(lib.tt_block_attn(ctypes.byref(self.attn_desc), tt._ptr(ly["q"]),
                                        tt._ptr(ly["k_ctx"]), tt._ptr(ly["v_ctx"]),
                                        tt._ptr(self.lens), tt._ptr(ly["k_blk"]),
                                        tt._ptr(ly["v_blk"]), tt._ptr(ly["out"]), None,
                                        self.attn_ws.ptr, self.attn_ws.nbytes, sp))
-            if ev_attn is not None:
-                ev_attn[i][1].record(stream)
+            if ev_attn is not None and i == len(self.layers) - 1:
+                ev_attn[1].record(stream)
         if ev_unmask is not None:
             ev_unmask[0].record(stream)
         tt.check(lib.tt_confidence_unmask(ctypes.byref(self.unmask_desc), tt._ptr(self.logits),
@@ -361,12 +362,13 @@ def run_ours(args, dist: Dist) -> dict:
     a = wl.a
     clocks = ClockSampler(dist.local)
     # With graphs (the default) the step is captured once per M steps (M the largest
-    # divisor of K up to 10) with an event pair around every kernel call inside the
-    # graph, and the K timed steps are K/M replays; the per-call times are those of
-    # the last replay's M steps, recorded inside the timed region.
+    # divisor of K up to 10), with event pairs inside the graph around the six attention
+    # calls and around the unmask call; the K timed steps are K/M replays, and the
+    # per-call times are those of the last replay's M steps, recorded inside the timed
+    # region.
     M = max(d for d in range(1, min(10, args.steps) + 1) if args.steps % d == 0)
     ev = lambda: torch.cuda.Event(enable_timing=True, external=not args.no_graph)  # noqa: E731
-    ev_attn = [[(ev(), ev()) for _ in wl.layers] for _ in range(M if not args.no_graph else args.steps)]
+    ev_attn = [(ev(), ev()) for _ in range(M if not args.no_graph else args.steps)]
     ev_unm = [(ev(), ev()) for _ in range(len(ev_attn))]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
@@ -399,7 +401,8 @@ def run_ours(args, dist: Dist) -> dict:
     clk = clocks.stop()
     ms = start.elapsed_time(end) / args.steps
     ms_max = dist.max(ms)
-    attn_ms = [s.elapsed_time(e) for row in ev_attn for (s, e) in row]
+    # the layers' calls run back to back between one event pair: the mean call time
+    attn_ms = [s.elapsed_time(e) / len(wl.layers) for (s, e) in ev_attn]
     unm_ms = [s.elapsed_time(e) for (s, e) in ev_unm]
     attn_avg = float(np.mean(attn_ms))
     unm_avg = float(np.mean(unm_ms))
@@ -418,7 +421,8 @@ def run_ours(args, dist: Dist) -> dict:
                     temperature=w.temperature, gamma=w.threshold,
                     step="block_init + 6 x tt_block_attn (distinct layer K/V) + tt_confidence_unmask",
                     launch=("CUDA graph of %d steps replayed %d times; per-call times from the "
-                            "events of the last replay" % (M, args.steps // M))
+                            "events of the last replay (one pair around the 6 attention calls, "
+                            "one around the unmask)" % (M, args.steps // M))
                     if not args.no_graph else "every kernel launched from the host",
                     l2="inputs larger than L2: 6 layer caches of %.0f MB visible K/V each" %
                        (ab / 1e6), parallelism=f"dp{n} (independent batches, no collective)"),

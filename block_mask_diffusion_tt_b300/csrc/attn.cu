@@ -89,8 +89,8 @@ struct Cfg {
     static constexpr uint32_t kIdescPV = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
                                          (uint32_t(D >> 3) << 17) | (uint32_t(128 >> 4) << 24);
     // barriers: full[S] empty[S] s_full[2][2] p_full[2][2] pv_done[2][2]
-    //           q_ready[2] fin[2] turn[2]
-    static constexpr int kNumBars = 2 * kStages + 18;
+    //           q_ready[2] fin[2] turn[2] q_tma[2]
+    static constexpr int kNumBars = 2 * kStages + 20;
     static constexpr int kBarOffset = kQOffset + 2 * kQHalfBytes;
     static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;  // tmem base, err, last[2]
     static constexpr int kPrefixOffset = kMiscOffset + 16;
@@ -117,6 +117,7 @@ struct AttnArgs {
     const float *q_scale;      // modulation: q' = q (1 + scale) + shift, [B, Hq, D] fp32, or null
     const float *q_shift;
     const float *o_gate;       // out = gate * attention, [B, Hq, D] fp32, or null
+    int q_tma;                 // the CTA's first segment's Q comes by TMA from the producer
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -348,6 +349,7 @@ struct Smem {
     __device__ uint32_t q_ready(int h) const { return bars + 8 * (S2 + 12 + h); }
     __device__ uint32_t fin(int h) const { return bars + 8 * (S2 + 14 + h); }
     __device__ uint32_t turn(int h) const { return bars + 8 * (S2 + 16 + h); }
+    __device__ uint32_t q_tma(int h) const { return bars + 8 * (S2 + 18 + h); }
     __device__ uint32_t q_tile(int h) const { return qbuf + h * Cfg<D>::kQHalfBytes; }
 };
 
@@ -368,7 +370,8 @@ __device__ __forceinline__ int page_at(const AttnArgs &a, int b, int tile, int L
 template <int D>
 __device__ void role_producer(const AttnArgs &a, Sched sch, const Smem<D> &sm,
                               const CUtensorMap *tkc, const CUtensorMap *tvc,
-                              const CUtensorMap *tkb, const CUtensorMap *tvb) {
+                              const CUtensorMap *tkb, const CUtensorMap *tvb,
+                              const CUtensorMap *tq) {
     using C = Cfg<D>;
     int stage = 0, nissued = 0;
     uint32_t phase = 0, issued = 0, last_par = 0;
@@ -378,7 +381,24 @@ __device__ void role_producer(const AttnArgs &a, Sched sch, const Smem<D> &sm,
     Seg s;
     bool ok = true;
     int next_page = 0;  // paged cache: page of the next context tile, read one tile ahead
+    uint32_t q_sent = 0;  // halves whose first Q came by TMA (drained at the end)
+    bool first = true;
     while (ok && sch.next(a, s)) {
+        if (first && a.q_tma) {
+            // The first segment's Q, ahead of every K/V tile: one 128-row box per half
+            // and 64-column chunk (rows (s, head) of the pair in order, s past S read as
+            // zeros), in the 128-byte swizzled K-major layout the Q K^T descriptor reads.
+            for (int h = 0; h < s.nh; ++h) {
+                mbar_expect_tx(sm.q_tma(h), C::kQHalfBytes);
+                const int s0 = (s.rg * kRows + h * 128) / a.G;
+#pragma unroll
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_4d(sm.q_tile(h) + c * C::kQRegion, tq, c * 64, s.g * a.G, s0, s.b,
+                                sm.q_tma(h), policy);
+                q_sent |= 1u << h;
+            }
+        }
+        first = false;
         if (a.page_of && s.tile0 < s.nctx) next_page = page_at(a, s.b, s.tile0, s.L);
         for (int it = 0; it < s.ntiles; ++it) {
             if (!mbar_wait(sm.empty(stage), phase ^ 1, sm.err, 1)) { ok = false; break; }
@@ -410,15 +430,18 @@ __device__ void role_producer(const AttnArgs &a, Sched sch, const Smem<D> &sm,
             issued |= 1u << stage;
             last_par = (last_par & ~(1u << stage)) | (phase << stage);
             if (++stage == C::kStages) { stage = 0; phase ^= 1; }
-            // At kernel start every SM asks for its first K/V tiles at once; the first
-            // segment's Q (loaded by the softmax warps) would queue behind them.  After
-            // one tile, wait for that Q before filling the rest of the ring.
-            if (ok && ++nissued == 1 && !mbar_wait(sm.q_ready(0), 0, sm.err, 1)) ok = false;
+            // At kernel start every SM asks for its first K/V tiles at once; a first Q
+            // loaded by the softmax warps would queue behind them.  Without the TMA Q,
+            // wait for that Q after one tile before filling the rest of the ring.
+            if (ok && !a.q_tma && ++nissued == 1 && !mbar_wait(sm.q_ready(0), 0, sm.err, 1))
+                ok = false;
         }
     }
     // no copy may still be landing when the CTA exits
     for (int st = 0; st < C::kStages; ++st)
         if (issued >> st & 1u) mbar_drain(sm.full(st), last_par >> st & 1u);
+    for (int h = 0; h < 2; ++h)
+        if (q_sent >> h & 1u) mbar_drain(sm.q_tma(h), 0);
 }
 
 // MMA warp of half h (warp 9 + h).  At step it it issues S_h = Q_h K^T for tile it
@@ -443,7 +466,9 @@ __device__ void role_mma(const AttnArgs &a, Sched sch, const Smem<D> &sm, uint32
     uint32_t phase = 0, qpar = 0, s_cnt = 0, p_cnt = 0;
     bool ok = true;
     Seg s;
+    int seg_idx = 0;  // segments of the CTA so far (the first one's Q may come by TMA)
     while (ok && sch.next(a, s)) {
+        const bool q_by_tma = a.q_tma && seg_idx++ == 0;
         if (h >= s.nh) {  // half unused in this segment: release each stage at once
             for (int it = 0; it < s.ntiles; ++it) {
                 if (!wait(sm.full(stage), phase)) { ok = false; break; }
@@ -474,8 +499,12 @@ __device__ void role_mma(const AttnArgs &a, Sched sch, const Smem<D> &sm, uint32
                     __syncwarp();
                 }
                 if (it == 0) {
-                    if (!wait(sm.q_ready(h), qpar)) { ok = false; break; }
-                    qpar ^= 1;
+                    if (q_by_tma) {
+                        if (!wait(sm.q_tma(h), 0)) { ok = false; break; }
+                    } else {
+                        if (!wait(sm.q_ready(h), qpar)) { ok = false; break; }
+                        qpar ^= 1;
+                    }
                 }
                 tc_fence_after();
                 const uint32_t d_s = tmem + C::colS(h, s_cnt & 1);
@@ -615,15 +644,19 @@ __device__ void role_softmax(const AttnArgs &a, Sched sch, const Smem<D> &sm, ui
         mbar_arrive(sm.q_ready(h));
     };
     // next segment in which this half takes part
+    int pulled = 0;  // segments of the CTA pulled so far
     auto next_mine = [&](Seg &n) -> bool {
-        while (sch.next(a, n))
+        while (sch.next(a, n)) {
+            ++pulled;
             if (h < n.nh) return true;
+        }
         return false;
     };
     bool ok = true;
     Seg s, nxt;
     bool have = next_mine(s);
-    if (have) load_q(s);
+    // the CTA's first segment's Q comes by TMA from the producer (when enabled)
+    if (have && !(a.q_tma && pulled == 1)) load_q(s);
     while (ok && have) {
         const bool valid = rl < s.rows;
         float m_run = -INFINITY, l_run = 0.f;
@@ -740,7 +773,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     block_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
                          const __grid_constant__ CUtensorMap tm_vc,
                          const __grid_constant__ CUtensorMap tm_kb,
-                         const __grid_constant__ CUtensorMap tm_vb, const AttnArgs a) {
+                         const __grid_constant__ CUtensorMap tm_vb,
+                         const __grid_constant__ CUtensorMap tm_q, const AttnArgs a) {
     using C = Cfg<D>;
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -829,6 +863,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(sm.fin(0), 1);
         mbar_init(sm.fin(1), 1);
+        mbar_init(sm.q_tma(0), 1);
+        mbar_init(sm.q_tma(1), 1);
         *sm.err = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -853,7 +889,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     sch.tend = static_cast<int64_t>(cta + 1) * T / P;
 
     if (warp == kProducerWarp) {
-        if (lane == 0) role_producer<D>(a, sch, sm, &tm_kc, &tm_vc, &tm_kb, &tm_vb);
+        if (lane == 0) role_producer<D>(a, sch, sm, &tm_kc, &tm_vc, &tm_kb, &tm_vb, &tm_q);
         __syncwarp();
     } else if (warp >= kMmaWarp) {
         role_mma<D>(a, sch, sm, tmem, warp - kMmaWarp);
@@ -1054,22 +1090,44 @@ tt_status make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, u
 // per-thread cache skips re-encoding them for repeated calls on the same buffers
 // (a decode loop calls every layer with the same caches step after step).
 struct MapKey {
-    const void *k_ctx, *v_ctx, *k_blk, *v_blk;
-    int32_t B, S, Hkv, Lmax, d, n_pages;  // n_pages > 0: paged context pools
-    int64_t kc[4], vc[4], kb[4], vb[4];
+    const void *k_ctx, *v_ctx, *k_blk, *v_blk, *q;  // q null: no Q map
+    int32_t B, S, Hq, Hkv, Lmax, d, n_pages;  // n_pages > 0: paged context pools
+    int64_t kc[4], vc[4], kb[4], vb[4], qs[4];
     bool operator==(const MapKey &o) const { return memcmp(this, &o, sizeof(MapKey)) == 0; }
 };
 struct MapEntry {
     MapKey key;
-    CUtensorMap kc, vc, kb, vb;
-    bool used;
+    CUtensorMap kc, vc, kb, vb, q;
+    bool used, has_q;
 };
 constexpr int kMapCache = 16;
 
 template <int D>
 tt_status encode_maps(const tt_attn_desc *d, const void *k_ctx, const void *v_ctx, const void *k_blk,
-                      const void *v_blk, int n_pages, MapEntry *e, const char *fn) {
+                      const void *v_blk, const void *q, int n_pages, MapEntry *e, const char *fn) {
     tt_status st;
+    // Q [B, S, Hq, d] as (d, Hq, S, B) with a box of 64 columns x G heads x 128/G block
+    // positions: one half's 128 rows of a pair.  A map the driver rejects only turns the
+    // TMA Q off (the softmax warps load it instead).
+    e->has_q = false;
+    if (q) {
+        const int G = d->Hq / d->Hkv;
+        EncodeTiledFn enc = encode_fn();
+        if (enc) {
+            const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(d->Hq),
+                                        static_cast<cuuint64_t>(d->S), static_cast<cuuint64_t>(d->B)};
+            const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d->q_strides[2]) * 2,
+                                           static_cast<cuuint64_t>(d->q_strides[1]) * 2,
+                                           static_cast<cuuint64_t>(d->q_strides[0]) * 2};
+            const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(G),
+                                       static_cast<cuuint32_t>(128 / G), 1};
+            const cuuint32_t estr[4] = {1, 1, 1, 1};
+            e->has_q = enc(&e->q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(q), dims,
+                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+        }
+    }
     const uint64_t B = d->B, S = d->S, Hkv = d->Hkv;
     // a paged cache is a pool [n_pages, Hkv, 64, d]: the map's rows are a page's 64 keys
     // and its outer dimension the page; otherwise [B, Hkv, Lmax, d]
@@ -1097,15 +1155,20 @@ tt_status encode_maps(const tt_attn_desc *d, const void *k_ctx, const void *v_ct
 
 
 template <int D>
-tt_status launch(const tt_attn_desc *d, const AttnArgs &a, const void *k_ctx, const void *v_ctx,
+tt_status launch(const tt_attn_desc *d, AttnArgs a, const void *k_ctx, const void *v_ctx,
                  const void *k_blk, const void *v_blk, cudaStream_t stream, const char *fn) {
     const int n_pages = a.page_of ? a.n_pages : 0;
+    // the first Q by TMA: unmodulated queries whose group size G divides 128 (a half's
+    // 128 rows are whole block positions)
+    const int G = d->Hq / d->Hkv;
+    const void *q_tma = (a.q_scale == nullptr && G <= 128 && 128 % G == 0) ? a.q : nullptr;
     thread_local MapEntry cache[kMapCache] = {};
     thread_local int next_slot = 0;
     MapKey key;
     memset(&key, 0, sizeof key);
-    key.k_ctx = k_ctx; key.v_ctx = v_ctx; key.k_blk = k_blk; key.v_blk = v_blk;
-    key.B = d->B; key.S = d->S; key.Hkv = d->Hkv; key.Lmax = d->Lmax; key.d = d->d;
+    key.k_ctx = k_ctx; key.v_ctx = v_ctx; key.k_blk = k_blk; key.v_blk = v_blk; key.q = q_tma;
+    key.B = d->B; key.S = d->S; key.Hq = d->Hq; key.Hkv = d->Hkv; key.Lmax = d->Lmax; key.d = d->d;
+    if (q_tma) memcpy(key.qs, d->q_strides, sizeof key.qs);
     key.n_pages = n_pages;
     memcpy(key.kc, d->kctx_strides, sizeof key.kc);
     memcpy(key.vc, d->vctx_strides, sizeof key.vc);
@@ -1116,7 +1179,7 @@ tt_status launch(const tt_attn_desc *d, const AttnArgs &a, const void *k_ctx, co
         if (cache[i].used && cache[i].key == key) hit = &cache[i];
     if (!hit) {
         tt_status st =
-            encode_maps<D>(d, k_ctx, v_ctx, k_blk, v_blk, n_pages, &cache[next_slot], fn);
+            encode_maps<D>(d, k_ctx, v_ctx, k_blk, v_blk, q_tma, n_pages, &cache[next_slot], fn);
         if (st != TT_OK) return st;
         cache[next_slot].key = key;
         cache[next_slot].used = true;
@@ -1124,6 +1187,8 @@ tt_status launch(const tt_attn_desc *d, const AttnArgs &a, const void *k_ctx, co
         next_slot = (next_slot + 1) % kMapCache;
     }
     const CUtensorMap &kc = hit->kc, &vc = hit->vc, &kb = hit->kb, &vb = hit->vb;
+    a.q_tma = hit->has_q ? 1 : 0;
+    const CUtensorMap &tq = hit->has_q ? hit->q : hit->kb;  // unused without the TMA Q
     static std::mutex mu;
     static bool configured[64] = {false};
     int dev = 0;
@@ -1139,7 +1204,7 @@ tt_status launch(const tt_attn_desc *d, const AttnArgs &a, const void *k_ctx, co
         }
     }
     block_attn_tc_kernel<D><<<a.P, kThreads, Cfg<D>::smem_bytes(a.npairs), stream>>>(kc, vc, kb,
-                                                                                    vb, a);
+                                                                                    vb, tq, a);
     tt_status st2 = cuda_status(cudaGetLastError(), "tt_block_attn launch");
     if (st2 != TT_OK) return st2;
     cudaLaunchConfig_t cfg = {};
