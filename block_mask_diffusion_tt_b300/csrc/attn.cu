@@ -388,13 +388,16 @@ __device__ void role_producer(const AttnArgs &a, Sched sch, const Smem<D> &sm,
             // The first segment's Q, ahead of every K/V tile: one 128-row box per half
             // and 64-column chunk (rows (s, head) of the pair in order, s past S read as
             // zeros), in the 128-byte swizzled K-major layout the Q K^T descriptor reads.
+            // The CTAs sharing a split pair load the same Q at about the same time: it
+            // is kept in L2 rather than evicted first like the K/V tiles.
+            const uint64_t q_policy = l2_evict_last();
             for (int h = 0; h < s.nh; ++h) {
                 mbar_expect_tx(sm.q_tma(h), C::kQHalfBytes);
                 const int s0 = (s.rg * kRows + h * 128) / a.G;
 #pragma unroll
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_4d(sm.q_tile(h) + c * C::kQRegion, tq, c * 64, s.g * a.G, s0, s.b,
-                                sm.q_tma(h), policy);
+                                sm.q_tma(h), q_policy);
                 q_sent |= 1u << h;
             }
         }
