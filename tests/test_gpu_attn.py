@@ -31,9 +31,10 @@ def test_ragged_prefix_lengths(lens, d):
 
 
 @pytest.mark.parametrize("S,Hq,Hkv", [(1, 4, 4), (4, 32, 2), (16, 32, 2), (16, 32, 1), (32, 32, 2),
-                                      (64, 32, 2), (7, 12, 3), (16, 16, 16)])
+                                      (64, 32, 2), (7, 12, 3), (16, 16, 16), (16, 9, 3), (16, 48, 2)])
 def test_block_sizes_and_head_groups(S, Hq, Hkv):
-    # S*Hq/Hkv above 256 spans several row groups
+    # S*Hq/Hkv above 256 spans several row groups; group sizes 3 and 24 do not divide 128,
+    # so the first Q of every CTA is loaded by the softmax warps instead of by TMA
     shape = synth.AttnShape(2, S, Hq, Hkv, 128, 300, lens=[300, 77])
     _gpu.check_attn(synth.attn_inputs(shape, seed=S * 100 + Hq), what=f"S={S} Hq={Hq} Hkv={Hkv}")
 
