@@ -16,6 +16,8 @@
 // and dots each row with every sequence's h, so W2 is read once for the whole batch.
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace tt {
@@ -102,15 +104,19 @@ extern "C" tt_status tt_adaln_single(const tt_adaln_desc *desc, const float *t, 
     if (rows > (int64_t(1) << 30)) return fail(TT_ERR_UNSUPPORTED, "%s: N too large", fn);
     AdaArgs a{t, w1, b1, w2, b2, embed, shift, scale, gate, d.B, d.F, d.Dh, d.N, d.layer};
     const size_t smem = sizeof(float) * (static_cast<size_t>(kAdaMaxB) * d.Dh + d.F);
-    static bool configured[64] = {false};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (smem > 48 * 1024 && dev >= 0 && dev < 64 && !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(adaln_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(sizeof(float) *
-                                                              (kAdaMaxB * kAdaMaxDh + kAdaMaxF)));
-        if (e != cudaSuccess) return cuda_status(e, "tt_adaln_single: smem attribute");
-        configured[dev] = true;
+    if (smem > 48 * 1024) {  // once per device: the largest dynamic shared memory the kernel takes
+        static std::once_flag once[64];
+        static cudaError_t set_err[64];
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return cuda_status(e, "tt_adaln_single");
+        if (dev < 0 || dev >= 64) return fail(TT_ERR_UNSUPPORTED, "%s: device index %d >= 64", fn, dev);
+        std::call_once(once[dev], [dev] {
+            set_err[dev] = cudaFuncSetAttribute(
+                adaln_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                static_cast<int>(sizeof(float) * (kAdaMaxB * kAdaMaxDh + kAdaMaxF)));
+        });
+        if (set_err[dev] != cudaSuccess) return cuda_status(set_err[dev], "tt_adaln_single: smem attribute");
     }
     const unsigned grid = static_cast<unsigned>((rows + kAdaThreads - 1) / kAdaThreads);
     adaln_kernel<<<grid, kAdaThreads, smem, static_cast<cudaStream_t>(stream)>>>(a);
