@@ -210,7 +210,8 @@ def run_loop(w: synth.Workload, n: int, time_it: bool = False):
                              f"steps used per block {mean_used:.2f} (loop ran {steps})")
                 records.append(dict(S=S, gamma=gamma, us_per_block=us,
                                     committed_tokens_per_s=a.B * S / us * 1e6,
-                                    steps_per_block=mean_used))
+                                    steps_per_block=mean_used,
+                                    max_steps_per_block=int(used.max())))
     return ("\n".join(lines), records, None) if time_it else None
 
 

@@ -233,7 +233,8 @@ class Workload:
 
 
 def workloads() -> dict:
-    """The five synthetic configurations (tiny, default, ragged 16K, long, sweep)."""
+    """The five synthetic configurations (tiny, default, ragged 16K, long, sweep), and a
+    uniform 16K side point (B=8, every prefix 16384 keys)."""
     return {
         "tiny": Workload("tiny: B=1 L=64 S=16 Hq=4 Hkv=1 d=64 V=1024 f32",
                          AttnShape(1, 16, 4, 1, 64, 64), 1024, "f32", 3.0, 0.0),
@@ -242,6 +243,8 @@ def workloads() -> dict:
         "ragged16k": Workload("ragged16k: B=32 L~U[1024,16384] S=16 Hq=32 Hkv=2 d=128 V=131072",
                               AttnShape(32, 16, 32, 2, 128, 16384, lens_range=(1024, 16384)),
                               131072, "bf16", 2.0, 0.6),
+        "uniform16k": Workload("uniform16k: B=8 L=16384 S=16 Hq=32 Hkv=2 d=128 V=131072",
+                               AttnShape(8, 16, 32, 2, 128, 16384), 131072, "bf16", 2.0, 0.6),
         "long": Workload("long: B=4 L=131072 S=16 Hq=32 Hkv=2 d=128 V=131072",
                          AttnShape(4, 16, 32, 2, 128, 131072), 131072, "bf16", 2.0, 0.6),
         "sweep": Workload("sweep: B=16 L=8192 S in {4..64} Hq=32 Hkv=2 d=128 V=131072",

@@ -184,6 +184,10 @@ def test_full_size_long_sampled():
     _sampled_full_size("long", lambda lens: [2])
 
 
+def test_full_size_uniform16k_sampled():
+    _sampled_full_size("uniform16k", lambda lens: [0, 7])
+
+
 def test_out_of_range_lengths_are_reported_and_clamped():
     """ctx_lens lives on the device, so the host cannot validate it: a length below 0 or
     above Lmax sets flag 8 of the workspace error word, and that sequence is computed
