@@ -61,7 +61,10 @@ constexpr int kMaxPairs = 4096;
 constexpr int kMinTiles = 4;  // smallest tile range worth a partial
 // Cost of starting a segment (Q load, pipeline refill, epilogue), in tile units: every
 // pair is charged this many extra units at its start when the tile ranges are cut.
-constexpr int kSegCost = 5;
+// Measured with the first Q by TMA (us per call, default / ragged16k / uniform 16K / long):
+// 5 gave 25.8 / 79.6 / 50.5 / 122.3, 7 gave 25.8 / 77.4 / 48.4 / 122.3, 10 gave
+// 26.9 / 78.5 / 48.7 / 121.4.
+constexpr int kSegCost = 7;
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kRescaleLog2 = 8.f;  // lazy rescale: O is rescaled when the max grows by > 2^8
 constexpr int kTmemCols = 512;
