@@ -611,8 +611,10 @@ struct Plan {
     int grid;  // CTAs
 };
 
-// Units of 32 KB, or 16 / 8 KB when a batch has too few units to give every CTA
-// (three per SM) at least four.
+// Units of 32 KB, or 16 / 8 KB when a batch has fewer units than CTAs (three per
+// SM).  Larger units win even for small batches: one CUDA-graph call on 128 rows x
+// 131072 bf16 took 10.5 us with 32 KB units against 14.6 us with the 8 KB units that
+// giving every CTA four units would take (64 rows: 8.0 against 15.3 us).
 Plan plan_for(const tt_unmask_desc *d) {
     const int es = d->logits_dtype == TT_F32 ? 4 : 2;
     const int64_t rows = static_cast<int64_t>(d->B) * d->S;
@@ -622,7 +624,7 @@ Plan plan_for(const tt_unmask_desc *d) {
     int bytes = kMaxUnitBytes;
     while (bytes > kMinUnitBytes) {
         const int64_t unit = bytes / es;
-        if (rows * ((d->V + unit - 1) / unit) >= 4 * ctas) break;
+        if (rows * ((d->V + unit - 1) / unit) >= ctas) break;
         bytes >>= 1;
     }
     Plan pl;

@@ -127,10 +127,12 @@ def test_empty_batch_is_noop():
 
 
 @pytest.mark.parametrize("B,S,V,dtype", [(40, 16, 4099, "bf16"), (40, 16, 20000, "f32"),
-                                         (8, 16, 131072, "bf16"), (40, 16, 70001, "bf16")])
+                                         (8, 16, 131072, "bf16"), (40, 16, 70001, "bf16"),
+                                         (2, 16, 131072, "bf16"), (1, 16, 131072, "bf16")])
 def test_grid_plans_and_unaligned_rows(B, S, V, dtype):
-    """Batches large enough for the kernel's largest per-thread chunk (16 vectors) and
-    small ones that use 8 or 4, with rows that start off a 16-byte boundary (odd V)."""
+    """Units of 32 KB, and (on 148 SMs, three CTAs each) the 16 KB and 8 KB units of
+    batches with fewer 32 KB units than CTAs (32 and 16 rows of 131072), with rows that
+    start off a 16-byte boundary (odd V)."""
     logits = synth.counter_logits(12, 0, B, S, V, 1.0, 0.3, dtype)
     _gpu.check_unmask(logits, dtype, 0.1, 0.8)
 
