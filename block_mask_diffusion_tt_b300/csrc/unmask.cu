@@ -6,9 +6,9 @@
 // confidence >= gamma, at least the most confident one; re-mask the rest.
 //
 // Design (HBM-bound: every logit of every masked row is read exactly once):
-//  * the vocabulary of every row is cut into units of at most 32 KB (8 or 16 KB
-//    for small batches, so that every SM gets several); three persistent CTAs
-//    per SM walk the units u = blockIdx.x + i * gridDim.x;
+//  * the vocabulary of every row is cut into units of 32 KB (16 or 8 KB only when
+//    a batch has fewer units than CTAs); three persistent CTAs per SM walk the
+//    units u = blockIdx.x + i * gridDim.x;
 //  * in each CTA one producer thread streams the units through a ring of
 //    shared-memory stages with TMA bulk copies (cp.async.bulk, full/empty
 //    mbarriers), 64 KB per CTA in flight; a unit of a row that is not masked is
